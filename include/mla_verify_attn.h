@@ -1,0 +1,128 @@
+/*
+ * mla_verify_attn.h -- C ABI of the GB300 (sm_103a) absorbed-MLA verify-attention library.
+ *
+ * The operation (pages by title):
+ *   "The Flash Attention Kernel That Had to Be Built: Designing sm_120 MLA
+ *   Verify for Blackwell Consumer GPUs", section "What Input Knowledge Is
+ *   Required to Understand This Message": each cache row is a 512-wide latent
+ *   kv_c followed by a 64-wide decoupled RoPE key k_pe; a query row is an
+ *   absorbed q_nope (512) and q_pe (64); score = q_nope . kv_c + q_pe . k_pe;
+ *   the latent kv_c is also the value; a draft query sees the keys its
+ *   candidate tree allows (paragraph "Speculative Decoding with DFlash"), the
+ *   others are set to -inf before a softmax ("Flash Attention Algorithm").
+ *   "The Decisive Microbench: When Theory Meets Silicon", section "The
+ *   KV-Split Solution": the key range is split across thread blocks whose
+ *   unnormalised partial states are merged by a second kernel with the
+ *   online-softmax combine.
+ *
+ * For stream b, draft i < q_len, head h < H, with prefix_b = seq_lens[b] - q_len:
+ *   visible(t) = t < prefix_b  or  (t < seq_lens[b] and bit (t - prefix_b) of mask row i)
+ *   s_t        = scale * (sum_d q_nope[b,i,h,d] kv[b,t,d] + sum_e q_rope[b,i,h,e] kv[b,t,512+e])
+ *   out[b,i,h] = sum_{visible t} softmax(s)_t * kv[b,t,0:512]
+ *   lse[b,i,h] = ln sum_{visible t} exp(s_t)          (-inf and out = 0 if nothing is visible)
+ *
+ * Conventions for every entry point:
+ *   - Device pointers unless stated otherwise; the caller owns all memory.
+ *     The library allocates no device memory.
+ *   - Calls are asynchronous on `stream`.  Argument errors are detected on the
+ *     host and returned before anything is launched.  Problems only the GPU can
+ *     see (a seq_lens value out of range, an internal wait that timed out) are
+ *     recorded in a per-device status word read by mla_verify_attn_last_device_error.
+ *   - bf16 tensors are passed as `const void*` holding IEEE bfloat16 values.
+ *   - Results are deterministic for fixed inputs, Smax and device.
+ */
+#ifndef MLA_VERIFY_ATTN_H
+#define MLA_VERIFY_ATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Status codes (returned by the entry points and by the device status). */
+enum mla_status {
+  MLA_OK = 0,
+  MLA_ERR_NULLPTR = -1,            /* a required pointer is NULL */
+  MLA_ERR_SHAPE = -2,              /* B, q_len, H or Smax outside the supported range */
+  MLA_ERR_ALIGN = -3,              /* a pointer misses its required alignment */
+  MLA_ERR_WORKSPACE = -4,          /* workspace smaller than mla_verify_attn_workspace_size() */
+  MLA_ERR_UNSUPPORTED_DEVICE = -5, /* current device is not sm_103 (GB300) or has no CUDA context */
+  MLA_ERR_LAUNCH = -6,             /* a kernel launch or tensor-map creation failed */
+  MLA_ERR_DEVICE_TIMEOUT = -7,     /* (device status) an internal pipeline wait gave up */
+  MLA_ERR_SEQLEN = -8,             /* (device status) some seq_lens[b] outside [q_len, Smax] */
+  MLA_ERR_ARG = -9                 /* any other invalid argument (e.g. non-finite scale) */
+};
+
+/*
+ * Bytes of scratch memory mla_verify_attn needs for these sizes on the
+ * current device (0 when the key range is not split).  The value depends only
+ * on (B, q_len, H, Smax) and the device's SM count.  Host-only; launches
+ * nothing.  Returns 0 as well for invalid sizes (mla_verify_attn then reports
+ * MLA_ERR_SHAPE).
+ * Scratch holds the per-split partial states of the key-range split (page
+ * "The Decisive Microbench: When Theory Meets Silicon", section "The KV-Split
+ * Solution"): [nsplit][B*q_len*H][512] fp32 accumulators followed by
+ * [nsplit][B*q_len*H][2] fp32 (running max, running sum).
+ */
+size_t mla_verify_attn_workspace_size(int B, int q_len, int H, int Smax);
+
+/*
+ * Verify attention for B streams of q_len draft queries over a latent cache.
+ *
+ *   q_nope_abs  [B, q_len, H, 512] bf16, contiguous; 16-byte aligned.
+ *   q_rope      [B, q_len, H, 64]  bf16, contiguous; 16-byte aligned.
+ *   kv          [B, Smax, 576]     bf16, contiguous; row = latent (512) | rope (64);
+ *               16-byte aligned.  Rows t < seq_lens[b] must be finite; rows at or
+ *               beyond seq_lens[b] may hold anything (NaN included) and are never used.
+ *   seq_lens    [B] int32: prefix_b + q_len, with q_len <= seq_lens[b] <= Smax.  The
+ *               drafts' own cache rows are rows prefix_b .. seq_lens[b]-1.
+ *   tree_mask   [B, q_len, ceil(q_len/32)] uint32; bit j (LSB first, word j/32) of row
+ *               i set <=> draft i sees draft j.  Bits >= q_len are ignored.
+ *   B >= 0, 1 <= q_len <= 64, 1 <= H, q_len*H*B < 2^31, 1 <= Smax < 2^24.
+ *   scale       finite float multiplying every score (e.g. 1/sqrt(192)).
+ *   out         [B, q_len, H, 512] fp32, normalised output; 16-byte aligned.
+ *   lse         [B, q_len, H] fp32, natural log-sum-exp of the scaled scores; 4-byte aligned.
+ *   workspace   device scratch of at least mla_verify_attn_workspace_size(B, q_len, H,
+ *               Smax) bytes, 256-byte aligned (may be NULL when that size is 0).  Its
+ *               contents on entry do not matter; it is not read after the call.
+ *   stream      CUDA stream (0 = legacy default stream).
+ *
+ * Returns MLA_OK after enqueuing the work, or a negative mla_status with nothing
+ * enqueued.  Calls that share a workspace must not overlap on the GPU.
+ */
+int mla_verify_attn(const void* q_nope_abs, const void* q_rope, const void* kv,
+                    const int32_t* seq_lens, const uint32_t* tree_mask, int B, int q_len, int H,
+                    int Smax, float scale, float* out, float* lse, void* workspace,
+                    size_t workspace_bytes, cudaStream_t stream);
+
+/*
+ * Synchronises `stream`, then returns and clears the current device's status
+ * word: MLA_OK, MLA_ERR_SEQLEN or MLA_ERR_DEVICE_TIMEOUT (the first recorded),
+ * or MLA_ERR_LAUNCH if the synchronisation itself failed.  The word is shared
+ * by all calls on the device since it was last read.
+ */
+int mla_verify_attn_last_device_error(cudaStream_t stream);
+
+/* Human-readable name of a status code (static string; never NULL). */
+const char* mla_verify_attn_strerror(int status);
+
+/*
+ * The split plan mla_verify_attn uses, for inspection and tests (host-only):
+ *   n_row_tiles  = ceil(q_len*H / 128) query-row tiles per stream,
+ *   nsplit       = number of key-range slices (1 = no split, no scratch),
+ *   chunk_tiles  = 64-key tiles per slice.
+ * `max_clusters` is the number of 2-CTA clusters that fit on the device at
+ * once (pass <= 0 to query the current device).  Honours the environment
+ * variable MLA_VERIFY_NSPLIT (a positive integer forces the slice count, for
+ * testing the split path on small inputs).  Returns MLA_OK or a status.
+ */
+int mla_verify_attn_plan(int B, int q_len, int H, int Smax, int max_clusters, int* n_row_tiles,
+                         int* nsplit, int* chunk_tiles);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MLA_VERIFY_ATTN_H */

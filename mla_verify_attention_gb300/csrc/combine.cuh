@@ -1,0 +1,68 @@
+// Merge of the per-slice partial states of the key-range split.
+//
+// Page "The Decisive Microbench: When Theory Meets Silicon", section "The
+// KV-Split Solution": a second kernel merges the slices' unnormalised
+// accumulators with the online-softmax combine.  For one query row with
+// slices s (running max m_s in log2-scaled units, running sum l_s, accumulator
+// O_s): M = max m_s, w_s = 2^(m_s - M), L = sum w_s l_s, out = sum w_s O_s / L,
+// lse = (M + log2 L) ln 2.  Slices with l_s = 0 are skipped (their O_s is 0).
+//
+// Memory-bound: one 128-thread block per query row, 16-byte loads and stores,
+// fully coalesced over the 512-wide rows.
+#pragma once
+#include <cstdint>
+#include <math_constants.h>
+
+#include "ptx.cuh"
+
+namespace mla {
+
+struct CombineParams {
+  const float* part_o;     // [nsplit][N][512]
+  const float2* part_ml;   // [nsplit][N]
+  const int32_t* seq_lens;
+  float* out;              // [N][512]
+  float* lse;              // [N]
+  int N;                   // B * q * H rows
+  int rows_per_stream;     // q * H
+  int q, Smax, nsplit, chunk_keys;
+};
+
+__global__ void __launch_bounds__(128) combine_kernel(const CombineParams p) {
+  const int row = blockIdx.x;
+  const int tid = threadIdx.x;
+  const int b = row / p.rows_per_stream;
+  const int S = p.seq_lens[b];
+  if (S < p.q || S > p.Smax) return;   // reported by the split kernel
+  const int ns = min(p.nsplit, (S + p.chunk_keys - 1) / p.chunk_keys);
+  float M = -CUDART_INF_F;
+  for (int s = 0; s < ns; ++s) {
+    const float2 ml = p.part_ml[static_cast<size_t>(s) * p.N + row];
+    if (ml.y > 0.f) M = fmaxf(M, ml.x);
+  }
+  float4* dst = reinterpret_cast<float4*>(p.out + static_cast<size_t>(row) * 512) + tid;
+  if (M == -CUDART_INF_F) {
+    *dst = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (tid == 0) p.lse[row] = -CUDART_INF_F;
+    return;
+  }
+  float L = 0.f;
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int s = 0; s < ns; ++s) {
+    const size_t idx = static_cast<size_t>(s) * p.N + row;
+    const float2 ml = p.part_ml[idx];
+    if (!(ml.y > 0.f)) continue;
+    const float w = ex2(ml.x - M);
+    L += w * ml.y;
+    const float4 o = reinterpret_cast<const float4*>(p.part_o + idx * 512)[tid];
+    acc.x += w * o.x;
+    acc.y += w * o.y;
+    acc.z += w * o.z;
+    acc.w += w * o.w;
+  }
+  const float inv = 1.f / L;
+  *dst = make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
+  if (tid == 0) p.lse[row] = (M + log2f(L)) * 0.6931471805599453f;
+}
+
+}  // namespace mla

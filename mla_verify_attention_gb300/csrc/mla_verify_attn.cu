@@ -1,0 +1,297 @@
+// Host side of the C ABI declared in include/mla_verify_attn.h: argument
+// checks, the split plan, TMA tensor maps and the two launches (split kernel,
+// then the merge of slice partials when the key range is split).
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <cmath>
+#include <cstdint>
+#include <cstdlib>
+#include <mutex>
+
+#include "mla_verify_attn.h"
+#include "combine.cuh"
+#include "verify_split.cuh"
+
+namespace {
+
+// Per-device status word (bits of mla::kStatus*), read and cleared by
+// mla_verify_attn_last_device_error().
+__device__ unsigned int g_mla_status;
+
+constexpr int kMaxDevices = 64;
+constexpr int kMinTilesPerSlice = 8;          // shortest slice worth a cluster's start-up
+constexpr int kTwoTermMaxKeys = 4096;         // streams up to this length send P as hi + lo
+constexpr size_t kSmemBytes = sizeof(mla::Smem) + 1024;   // + manual 1 KB alignment
+
+struct DeviceInfo {
+  bool ready = false;
+  int status = MLA_ERR_UNSUPPORTED_DEVICE;
+  int sms = 0;
+  int max_clusters = 0;
+  unsigned int* status_word = nullptr;
+  PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
+};
+
+std::mutex g_mutex;
+DeviceInfo g_devices[kMaxDevices];
+
+int device_info(DeviceInfo** out) {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+    cudaGetLastError();
+    return MLA_ERR_UNSUPPORTED_DEVICE;
+  }
+  std::lock_guard<std::mutex> lock(g_mutex);
+  DeviceInfo& d = g_devices[dev];
+  if (!d.ready) {
+    d.ready = true;
+    int major = 0, minor = 0, sms = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+      cudaGetLastError();
+      d.status = MLA_ERR_UNSUPPORTED_DEVICE;
+    } else if (major != 10 || minor != 3) {
+      d.status = MLA_ERR_UNSUPPORTED_DEVICE;   // the kernels are built for sm_103a only
+    } else {
+      d.sms = sms;
+      d.status = MLA_OK;
+      void* fn = nullptr;
+      cudaDriverEntryPointQueryResult q;
+      if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
+                                           cudaEnableDefault, &q) != cudaSuccess ||
+          q != cudaDriverEntryPointSuccess || fn == nullptr)
+        d.status = MLA_ERR_UNSUPPORTED_DEVICE;
+      d.encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+      if (d.status == MLA_OK &&
+          cudaFuncSetAttribute(mla::verify_split_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               static_cast<int>(kSmemBytes)) != cudaSuccess)
+        d.status = MLA_ERR_LAUNCH;
+      if (d.status == MLA_OK) {
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(2 * sms, 1, 1);
+        cfg.blockDim = dim3(mla::kThreads, 1, 1);
+        cfg.dynamicSmemBytes = kSmemBytes;
+        int n = 0;
+        if (cudaOccupancyMaxActiveClusters(&n, mla::verify_split_kernel, &cfg) != cudaSuccess ||
+            n < 1)
+          n = sms / 2;
+        d.max_clusters = n;
+        void* sym = nullptr;
+        if (cudaGetSymbolAddress(&sym, g_mla_status) != cudaSuccess) d.status = MLA_ERR_LAUNCH;
+        d.status_word = static_cast<unsigned int*>(sym);
+      }
+      cudaGetLastError();
+    }
+  }
+  *out = &d;
+  return d.status;
+}
+
+bool shape_ok(int B, int q, int H, int Smax) {
+  if (B < 0 || q < 1 || q > 64 || H < 1 || Smax < 1 || Smax >= (1 << 24)) return false;
+  const long long rows = static_cast<long long>(B) * q * H;
+  return rows < (1LL << 31);
+}
+
+int plan(int B, int q, int H, int Smax, int max_clusters, int* n_rt, int* nsplit, int* chunk) {
+  if (!shape_ok(B, q, H, Smax) || max_clusters < 1) return MLA_ERR_SHAPE;
+  const int rows = q * H;
+  const int nrt = (rows + mla::kRows - 1) / mla::kRows;
+  const int tiles = (Smax + mla::kKeys - 1) / mla::kKeys;
+  const long long base = static_cast<long long>(B > 0 ? B : 1) * nrt;
+  long long ns;
+  const char* env = std::getenv("MLA_VERIFY_NSPLIT");
+  const long long forced = env ? std::atoll(env) : 0;
+  int ct;
+  if (forced > 0) {
+    ns = forced < tiles ? forced : tiles;
+    ct = static_cast<int>((tiles + ns - 1) / ns);
+  } else {
+    if (base >= max_clusters) {
+      ns = 1;
+    } else if (B <= 1) {
+      ns = max_clusters / base;                       // one wave of clusters
+    } else {
+      ns = (4LL * max_clusters + base - 1) / base;    // ragged streams: smaller slices
+    }
+    ct = static_cast<int>((tiles + ns - 1) / ns);
+    if (ct < kMinTilesPerSlice) ct = kMinTilesPerSlice;
+  }
+  if (ct > tiles) ct = tiles;
+  ns = (tiles + ct - 1) / ct;
+  *n_rt = nrt;
+  *nsplit = static_cast<int>(ns);
+  *chunk = ct;
+  return MLA_OK;
+}
+
+size_t workspace_bytes_for(int B, int q, int H, int nsplit) {
+  if (nsplit <= 1) return 0;
+  const size_t n = static_cast<size_t>(B) * q * H;
+  return static_cast<size_t>(nsplit) * n * (512 * sizeof(float) + sizeof(float2));
+}
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+int encode(DeviceInfo* d, CUtensorMap* map, const void* base, int rank, const cuuint64_t* dims,
+           const cuuint64_t* strides, const cuuint32_t* box) {
+  const cuuint32_t elem[3] = {1, 1, 1};
+  const CUresult r = d->encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, const_cast<void*>(base),
+                               dims, strides, box, elem, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                               CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? MLA_OK : MLA_ERR_LAUNCH;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* mla_verify_attn_strerror(int status) {
+  switch (status) {
+    case MLA_OK: return "MLA_OK";
+    case MLA_ERR_NULLPTR: return "MLA_ERR_NULLPTR: a required pointer is NULL";
+    case MLA_ERR_SHAPE: return "MLA_ERR_SHAPE: B, q_len, H or Smax outside the supported range";
+    case MLA_ERR_ALIGN: return "MLA_ERR_ALIGN: a pointer misses its required alignment";
+    case MLA_ERR_WORKSPACE: return "MLA_ERR_WORKSPACE: workspace smaller than required";
+    case MLA_ERR_UNSUPPORTED_DEVICE: return "MLA_ERR_UNSUPPORTED_DEVICE: current device is not sm_103";
+    case MLA_ERR_LAUNCH: return "MLA_ERR_LAUNCH: kernel launch or tensor-map creation failed";
+    case MLA_ERR_DEVICE_TIMEOUT: return "MLA_ERR_DEVICE_TIMEOUT: a device pipeline wait gave up";
+    case MLA_ERR_SEQLEN: return "MLA_ERR_SEQLEN: seq_lens[b] outside [q_len, Smax]";
+    case MLA_ERR_ARG: return "MLA_ERR_ARG: invalid argument";
+    default: return "unknown mla_verify_attn status";
+  }
+}
+
+int mla_verify_attn_plan(int B, int q_len, int H, int Smax, int max_clusters, int* n_row_tiles,
+                         int* nsplit, int* chunk_tiles) {
+  if (!n_row_tiles || !nsplit || !chunk_tiles) return MLA_ERR_NULLPTR;
+  if (!shape_ok(B, q_len, H, Smax)) return MLA_ERR_SHAPE;
+  if (max_clusters <= 0) {
+    DeviceInfo* d = nullptr;
+    const int st = device_info(&d);
+    if (st != MLA_OK) return st;
+    max_clusters = d->max_clusters;
+  }
+  return plan(B, q_len, H, Smax, max_clusters, n_row_tiles, nsplit, chunk_tiles);
+}
+
+size_t mla_verify_attn_workspace_size(int B, int q_len, int H, int Smax) {
+  if (!shape_ok(B, q_len, H, Smax)) return 0;
+  DeviceInfo* d = nullptr;
+  if (device_info(&d) != MLA_OK) return 0;
+  int nrt, ns, ct;
+  if (plan(B, q_len, H, Smax, d->max_clusters, &nrt, &ns, &ct) != MLA_OK) return 0;
+  return workspace_bytes_for(B, q_len, H, ns);
+}
+
+int mla_verify_attn(const void* q_nope_abs, const void* q_rope, const void* kv,
+                    const int32_t* seq_lens, const uint32_t* tree_mask, int B, int q_len, int H,
+                    int Smax, float scale, float* out, float* lse, void* workspace,
+                    size_t workspace_bytes, cudaStream_t stream) {
+  if (!shape_ok(B, q_len, H, Smax)) return MLA_ERR_SHAPE;
+  if (!std::isfinite(scale)) return MLA_ERR_ARG;
+  if (B == 0) return MLA_OK;
+  if (!q_nope_abs || !q_rope || !kv || !seq_lens || !tree_mask || !out || !lse)
+    return MLA_ERR_NULLPTR;
+  if (!aligned(q_nope_abs, 16) || !aligned(q_rope, 16) || !aligned(kv, 16) || !aligned(out, 16) ||
+      !aligned(lse, 4) || !aligned(seq_lens, 4) || !aligned(tree_mask, 4) ||
+      (workspace && !aligned(workspace, 256)))
+    return MLA_ERR_ALIGN;
+
+  DeviceInfo* d = nullptr;
+  int st = device_info(&d);
+  if (st != MLA_OK) return st;
+  int nrt, ns, ct;
+  st = plan(B, q_len, H, Smax, d->max_clusters, &nrt, &ns, &ct);
+  if (st != MLA_OK) return st;
+  const size_t need = workspace_bytes_for(B, q_len, H, ns);
+  if (need > 0 && (!workspace || workspace_bytes < need)) return MLA_ERR_WORKSPACE;
+
+  const long long rows = static_cast<long long>(B) * q_len * H;
+  CUtensorMap map_qn, map_qr, map_kv;
+  {
+    const cuuint64_t dims[2] = {512, static_cast<cuuint64_t>(rows)};
+    const cuuint64_t strides[1] = {512 * 2};
+    const cuuint32_t box[2] = {64, mla::kRows};
+    if (encode(d, &map_qn, q_nope_abs, 2, dims, strides, box) != MLA_OK) return MLA_ERR_LAUNCH;
+  }
+  {
+    const cuuint64_t dims[2] = {64, static_cast<cuuint64_t>(rows)};
+    const cuuint64_t strides[1] = {64 * 2};
+    const cuuint32_t box[2] = {64, mla::kRows};
+    if (encode(d, &map_qr, q_rope, 2, dims, strides, box) != MLA_OK) return MLA_ERR_LAUNCH;
+  }
+  {
+    const cuuint64_t dims[3] = {576, static_cast<cuuint64_t>(Smax), static_cast<cuuint64_t>(B)};
+    const cuuint64_t strides[2] = {576 * 2, static_cast<cuuint64_t>(Smax) * 576 * 2};
+    const cuuint32_t box[3] = {64, mla::kKeys, 1};
+    if (encode(d, &map_kv, kv, 3, dims, strides, box) != MLA_OK) return MLA_ERR_LAUNCH;
+  }
+
+  mla::SplitParams p;
+  p.seq_lens = seq_lens;
+  p.mask = tree_mask;
+  p.out = out;
+  p.lse = lse;
+  p.part_o = static_cast<float*>(workspace);
+  p.part_ml = ns > 1 ? reinterpret_cast<float2*>(static_cast<char*>(workspace) +
+                                                 static_cast<size_t>(ns) * rows * 512 * 4)
+                     : nullptr;
+  p.status = d->status_word;
+  p.B = B;
+  p.q = q_len;
+  p.H = H;
+  p.Smax = Smax;
+  p.n_rt = nrt;
+  p.nsplit = ns;
+  p.chunk_tiles = ct;
+  p.two_term_max_keys = kTwoTermMaxKeys;
+  p.scale_log2 = scale * 1.4426950408889634f;
+
+  const long long units = static_cast<long long>(B) * nrt * ns;
+  if (2 * units >= (1LL << 31)) return MLA_ERR_SHAPE;
+  mla::verify_split_kernel<<<static_cast<unsigned>(2 * units), mla::kThreads, kSmemBytes, stream>>>(
+      map_qn, map_qr, map_kv, p);
+  if (cudaGetLastError() != cudaSuccess) return MLA_ERR_LAUNCH;
+  if (ns > 1) {
+    mla::CombineParams c;
+    c.part_o = p.part_o;
+    c.part_ml = p.part_ml;
+    c.seq_lens = seq_lens;
+    c.out = out;
+    c.lse = lse;
+    c.N = static_cast<int>(rows);
+    c.rows_per_stream = q_len * H;
+    c.q = q_len;
+    c.Smax = Smax;
+    c.nsplit = ns;
+    c.chunk_keys = ct * mla::kKeys;
+    mla::combine_kernel<<<static_cast<unsigned>(rows), 128, 0, stream>>>(c);
+    if (cudaGetLastError() != cudaSuccess) return MLA_ERR_LAUNCH;
+  }
+  return MLA_OK;
+}
+
+int mla_verify_attn_last_device_error(cudaStream_t stream) {
+  DeviceInfo* d = nullptr;
+  const int st = device_info(&d);
+  if (st != MLA_OK) return st;
+  if (cudaStreamSynchronize(stream) != cudaSuccess) {
+    cudaGetLastError();
+    return MLA_ERR_LAUNCH;
+  }
+  unsigned int v = 0;
+  if (cudaMemcpyFromSymbol(&v, g_mla_status, sizeof v) != cudaSuccess) return MLA_ERR_LAUNCH;
+  const unsigned int zero = 0;
+  if (v != 0 && cudaMemcpyToSymbol(g_mla_status, &zero, sizeof zero) != cudaSuccess)
+    return MLA_ERR_LAUNCH;
+  if (v & mla::kStatusSeqLen) return MLA_ERR_SEQLEN;
+  if (v & mla::kStatusTimeout) return MLA_ERR_DEVICE_TIMEOUT;
+  return MLA_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,623 @@
+// Split kernel of absorbed-MLA verify attention on sm_103a.
+//
+// What it computes (pages by title):
+//   "The Flash Attention Kernel That Had to Be Built: Designing sm_120 MLA
+//   Verify for Blackwell Consumer GPUs", section "What Input Knowledge Is
+//   Required to Understand This Message": score = q_nope . kv_c + q_pe . k_pe
+//   over a 576-wide cache row, tree-masked, softmax, output = weighted sum of
+//   the 512-wide latent; online softmax over key tiles ("Flash Attention
+//   Algorithm").  "The Decisive Microbench: When Theory Meets Silicon",
+//   section "The KV-Split Solution": each block works on one slice of the key
+//   range and leaves its unnormalised accumulator and statistics in scratch
+//   for a second, merging kernel.
+//
+// How (GB300 design, not the pages' sm_120 one).  In absorbed MLA every head
+// reads the same latent cache, so the 64 heads x q_len drafts of a stream are
+// the M dimension of one dense contraction.  One work unit is 128 query rows
+// (flattened (draft, head) rows of one stream) against one key slice, run by a
+// cluster of two CTAs on two SMs:
+//
+//   S CTA (cluster rank 0): Q[128 x 576] bf16 lives in tensor memory and is
+//     the A operand of S = Q K^T (tcgen05.mma, M=128, N=64 keys, K=576, fp32
+//     accumulator in tensor memory, double-buffered).  Four softmax warps own
+//     one row each per thread: scale, tree mask, running max with lazy
+//     rescaling, exp2, running sum, and bf16 P.  P (plus per-row rescale
+//     factors) is pushed into the O CTA's shared memory with st.async.
+//   O CTA (cluster rank 1): owns the 128 x 512 fp32 accumulator, i.e. all 512
+//     tensor-memory columns.  Its MMA warp runs O += P V with P (K-major) and
+//     V (MN-major, the latent part of the same cache rows) from shared memory,
+//     N=256 per instruction.  Four warps rescale O rows when the S CTA raised
+//     a row's max, zero cache rows past the stream end, and write the result.
+//
+// Each CTA streams the cache slice it needs straight from HBM/L2 with TMA
+// (128-byte swizzle).  P is rounded to bf16 because V is bf16 in the cache;
+// for short streams (where a few keys carry most of the weight) P is sent as
+// two bf16 terms hi + lo and the PV product is issued once per term.
+#pragma once
+#include <cstdint>
+#include <cstdio>
+#include <cuda.h>
+#include <math_constants.h>
+
+#include "ptx.cuh"
+
+namespace mla {
+
+constexpr int kDl = 512;
+constexpr int kDr = 64;
+constexpr int kRows = 128;                       // query rows per unit (MMA M)
+constexpr int kKeys = 64;                        // keys per tile (QK N, PV K)
+constexpr int kChunk = kKeys * 64 * 2;           // 8 KB: 64 keys x 64 dims bf16
+constexpr int kQChunk = kRows * 64 * 2;          // 16 KB: 128 rows x 64 dims bf16
+constexpr int kKChunks = 9;                      // 576 / 64
+constexpr int kVChunks = 8;                      // 512 / 64
+constexpr int kKSlots = 24;                      // S CTA key-chunk ring
+constexpr int kVSlots = 2;                       // O CTA value-tile ring
+constexpr int kVTile = kVChunks * kChunk;        // 64 KB
+constexpr int kPTerm = kRows * kKeys * 2;        // 16 KB per P term buffer
+constexpr int kThreads = 256;
+constexpr int kRingBytes = 192 * 1024;
+constexpr int kPOffset = kVSlots * kVTile;       // P buffers follow the two V tiles
+constexpr uint32_t kQCols = 288;                 // Q in tensor memory: 576 bf16 = 288 cols
+constexpr float kLazyRescale = 8.0f;             // log2 units: keep the max unless it grows by 2^8
+constexpr uint64_t kWaitNs = 2000000000ull;      // bounded waits: 2 s
+
+constexpr uint32_t kIdescQK = idesc_bf16_f32(128, 64, 0, 0);
+constexpr uint32_t kIdescPV = idesc_bf16_f32(128, 256, 0, 1);
+
+enum : uint32_t { kCmdDone = 0xFFFFFFFFu, kCmdZeroTail = 0x80000000u };
+
+// Device status bits (first error wins in the host's report).
+enum : uint32_t { kStatusSeqLen = 1u, kStatusTimeout = 2u };
+
+struct SplitParams {
+  const int32_t* seq_lens;
+  const uint32_t* mask;
+  float* out;
+  float* lse;
+  float* part_o;      // [nsplit][B*rows][512]
+  float2* part_ml;    // [nsplit][B*rows]
+  unsigned int* status;
+  int B, q, H, Smax;
+  int n_rt, nsplit, chunk_tiles;
+  int two_term_max_keys;
+  float scale_log2;   // scale * log2(e)
+};
+
+struct __align__(1024) Smem {
+  uint8_t ring[kRingBytes];
+  float alpha[2][kRows];
+  uint32_t flags[2][4];
+  float2 ml[kRows];
+  uint64_t kfull[kKSlots], kempty[kKSlots];
+  uint64_t qfull, qready;
+  uint64_t sfull[2], sempty[2];
+  uint64_t pempty[2];
+  uint64_t vfull[kVSlots], vempty[kVSlots];
+  uint64_t pfull[2];
+  uint64_t odone, corrgo, corrdone, mlfull, drain;
+  uint32_t tmem_base;
+  uint32_t abort_flag;
+  uint32_t cmd;
+};
+
+struct Unit {
+  int b, rt, sp;
+  int S, prefix;
+  int k0, k1, ntiles;
+  int rows_total, row0, valid_rows;
+  bool empty, two_term, zero_tail;
+};
+
+__device__ __forceinline__ Unit decode_unit(const SplitParams& p) {
+  Unit u;
+  const int unit = blockIdx.x >> 1;
+  u.rt = unit % p.n_rt;
+  const int t = unit / p.n_rt;
+  u.sp = t % p.nsplit;
+  u.b = t / p.nsplit;
+  u.S = p.seq_lens[u.b];
+  u.prefix = u.S - p.q;
+  u.rows_total = p.q * p.H;
+  u.row0 = u.rt * kRows;
+  u.valid_rows = min(kRows, u.rows_total - u.row0);
+  const bool bad = u.S < p.q || u.S > p.Smax;
+  u.k0 = u.sp * p.chunk_tiles * kKeys;
+  u.k1 = min(u.S, u.k0 + p.chunk_tiles * kKeys);
+  u.empty = bad || u.k0 >= u.k1;
+  u.ntiles = u.empty ? 0 : (u.k1 - u.k0 + kKeys - 1) / kKeys;
+  u.two_term = u.S <= p.two_term_max_keys;
+  u.zero_tail = !u.empty && ((u.k1 - u.k0) % kKeys) != 0;
+  return u;
+}
+
+// Bounded wait that also gives up as soon as another warp of the CTA aborted.
+// On a timeout the kernel records the error, prints which wait gave up (site
+// number, cluster rank, warp, parity) and makes the other warps unwind.
+template <bool kCluster = false>
+__device__ __noinline__ bool wait_slow(Smem& sm, uint32_t bar, uint32_t parity,
+                                       const SplitParams& p, int site) {
+  const uint64_t t0 = globaltimer_ns();
+  while (true) {
+    if (kCluster ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity)) return true;
+    if (*reinterpret_cast<volatile uint32_t*>(&sm.abort_flag)) return false;
+    if (globaltimer_ns() - t0 > kWaitNs) {
+      atomicOr(p.status, kStatusTimeout);
+      *reinterpret_cast<volatile uint32_t*>(&sm.abort_flag) = 1u;
+      printf("mla_verify_attn: wait timed out: site %d rank %u block %d warp %d parity %u\n", site,
+             cluster_ctarank(), static_cast<int>(blockIdx.x), static_cast<int>(threadIdx.x >> 5),
+             parity);
+      return false;
+    }
+  }
+}
+
+template <bool kCluster = false>
+__device__ __forceinline__ bool wait_or_abort(Smem& sm, uint32_t bar, uint32_t parity,
+                                              const SplitParams& p, int site) {
+  if (kCluster ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity)) return true;
+  return wait_slow<kCluster>(sm, bar, parity, p, site);
+}
+
+// Before a CTA exits, every TMA copy it issued must have landed: wait for the
+// last phase each ring slot was armed for.  Consumed phases return at once.
+__device__ __forceinline__ void drain_ring(const uint64_t* full, int nslots, int n_issued) {
+  for (int n = n_issued - 1; n >= 0 && n >= n_issued - nslots; --n)
+    mbar_wait(smem_u32(&full[n % nslots]), (n / nslots) & 1, kWaitNs / 2);
+}
+
+// ============================================================ S CTA roles
+
+__device__ __forceinline__ void s_producer(Smem& sm, const Unit& u, const SplitParams& p,
+                                           const CUtensorMap* map_qn, const CUtensorMap* map_qr,
+                                           const CUtensorMap* map_kv, int& n_issued) {
+  const uint32_t ring = smem_u32(sm.ring);
+  const uint32_t qfull = smem_u32(&sm.qfull);
+  // Q rows of this unit: 8 latent chunks + 1 rope chunk of [128 rows x 64 dims].
+  const int y = u.b * u.rows_total + u.row0;
+  mbar_arrive_expect_tx(qfull, kKChunks * kQChunk);
+  for (int c = 0; c < kVChunks; ++c) tma_load_2d(ring + c * kQChunk, map_qn, 64 * c, y, qfull);
+  tma_load_2d(ring + kVChunks * kQChunk, map_qr, 0, y, qfull);
+  // The Q staging area overlaps the first ring slots: wait until the softmax
+  // warps have moved Q into tensor memory.
+  if (!wait_or_abort(sm, smem_u32(&sm.qready), 0, p, 1)) return;
+  fence_proxy_async();
+  int n = 0;
+  for (int j = 0; j < u.ntiles; ++j) {
+    const int key = u.k0 + j * kKeys;
+    for (int c = 0; c < kKChunks; ++c, ++n) {
+      const int slot = n % kKSlots;
+      const uint32_t ph = (n / kKSlots) & 1;
+      if (!wait_or_abort(sm, smem_u32(&sm.kempty[slot]), ph ^ 1, p, 2)) return;
+      const uint32_t full = smem_u32(&sm.kfull[slot]);
+      mbar_arrive_expect_tx(full, kChunk);
+      tma_load_3d(ring + slot * kChunk, map_kv, 64 * c, key, u.b, full);
+      n_issued = n + 1;
+    }
+  }
+}
+
+__device__ __forceinline__ void s_mma(Smem& sm, const Unit& u, const SplitParams& p,
+                                      uint32_t tmem) {
+  const uint32_t ring = smem_u32(sm.ring);
+  if (!wait_or_abort(sm, smem_u32(&sm.qready), 0, p, 3)) return;
+  tc_fence_after();
+  int n = 0;
+  for (int j = 0; j < u.ntiles; ++j) {
+    const int buf = j & 1;
+    if (!wait_or_abort(sm, smem_u32(&sm.sempty[buf]), ((j >> 1) & 1) ^ 1, p, 4)) return;
+    tc_fence_after();
+    const uint32_t d = tmem + kQCols + 64 * buf;
+    for (int c = 0; c < kKChunks; ++c, ++n) {
+      const int slot = n % kKSlots;
+      if (!wait_or_abort(sm, smem_u32(&sm.kfull[slot]), (n / kKSlots) & 1, p, 5)) return;
+      tc_fence_after();
+#pragma unroll
+      for (int ks = 0; ks < 4; ++ks) {
+        const uint64_t bdesc = sdesc_sw128(ring + slot * kChunk + ks * 32, 16, 1024);
+        mma_ts(d, tmem + c * 32 + ks * 8, bdesc, kIdescQK, (c | ks) != 0);
+      }
+      mma_commit(smem_u32(&sm.kempty[slot]));
+    }
+    mma_commit(smem_u32(&sm.sfull[buf]));
+  }
+}
+
+__device__ __forceinline__ void s_softmax(Smem& sm, const Unit& u, const SplitParams& p,
+                                          uint32_t tmem, int wq, int lane) {
+  const int r = wq * 32 + lane;                     // row of the unit == tensor-memory lane
+  const uint32_t lane_base = static_cast<uint32_t>(wq * 32) << 16;
+  const int R = u.row0 + r;
+  const bool row_valid = r < u.valid_rows;
+  uint64_t mask64 = 0;
+  if (row_valid) {
+    const int i = R / p.H;
+    const int words = (p.q + 31) >> 5;
+    const uint32_t* mrow = p.mask + (static_cast<size_t>(u.b) * p.q + i) * words;
+    mask64 = mrow[0];
+    if (words > 1) mask64 |= static_cast<uint64_t>(mrow[1]) << 32;
+    if (p.q < 64) mask64 &= (1ull << p.q) - 1ull;
+  }
+
+  // ---- Q: staging shared memory -> registers -> tensor memory
+  if (!wait_or_abort(sm, smem_u32(&sm.qfull), 0, p, 6)) return;
+  for (int c = 0; c < kKChunks; ++c) {
+    const uint8_t* src = sm.ring + c * kQChunk + r * 128;
+    uint32_t v[32];
+#pragma unroll
+    for (int q4 = 0; q4 < 8; ++q4) {
+      const uint4 x = *reinterpret_cast<const uint4*>(src + ((q4 ^ (r & 7)) << 4));
+      v[4 * q4 + 0] = x.x;
+      v[4 * q4 + 1] = x.y;
+      v[4 * q4 + 2] = x.z;
+      v[4 * q4 + 3] = x.w;
+    }
+    MLA_TMEM_ST_32x32b_X32(tmem + lane_base + c * 32, v);
+  }
+  tmem_st_wait();
+  tc_fence_before();
+  __syncwarp();
+  if (lane == 0) mbar_arrive(smem_u32(&sm.qready));
+
+  // ---- peer (O CTA) addresses
+  const uint32_t peer = 1;
+  const uint32_t p_remote = mapa_shared(smem_u32(sm.ring + kPOffset), peer);
+  const uint32_t alpha_remote = mapa_shared(smem_u32(&sm.alpha[0][0]), peer);
+  const uint32_t flags_remote = mapa_shared(smem_u32(&sm.flags[0][0]), peer);
+  const uint32_t pfull_remote0 = mapa_shared(smem_u32(&sm.pfull[0]), peer);
+  const uint32_t pfull_remote1 = mapa_shared(smem_u32(&sm.pfull[1]), peer);
+  const uint32_t ml_remote = mapa_shared(smem_u32(&sm.ml[0]), peer);
+  const uint32_t mlfull_remote = mapa_shared(smem_u32(&sm.mlfull), peer);
+
+  const float sl2 = p.scale_log2;
+  float m_used = -CUDART_INF_F;   // log2-scaled running max actually used for P
+  float l = 0.f;                  // running sum of P (as fed to the PV product)
+
+  for (int j = 0; j < u.ntiles; ++j) {
+    const int buf = j & 1;
+    if (!wait_or_abort(sm, smem_u32(&sm.sfull[buf]), (j >> 1) & 1, p, 7)) return;
+    tc_fence_after();
+    uint32_t sr[64];
+    MLA_TMEM_LD_32x32b_X32(tmem + lane_base + kQCols + 64 * buf, sr);
+    MLA_TMEM_LD_32x32b_X32(tmem + lane_base + kQCols + 64 * buf + 32, (sr + 32));
+    tmem_ld_wait();
+    tc_fence_before();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(smem_u32(&sm.sempty[buf]));
+
+    const int key0 = u.k0 + j * kKeys;
+    float y[64];
+    const bool all_visible = row_valid && (key0 + kKeys <= u.prefix);
+    if (all_visible) {
+#pragma unroll
+      for (int c = 0; c < 64; ++c) y[c] = __uint_as_float(sr[c]) * sl2;
+    } else {
+#pragma unroll
+      for (int c = 0; c < 64; ++c) {
+        const int t = key0 + c;
+        bool vis = row_valid && (t < u.S);
+        if (vis && t >= u.prefix) vis = (mask64 >> (t - u.prefix)) & 1ull;
+        y[c] = vis ? __uint_as_float(sr[c]) * sl2 : -CUDART_INF_F;
+      }
+    }
+    float mt = y[0];
+#pragma unroll
+    for (int c = 1; c < 64; ++c) mt = fmaxf(mt, y[c]);
+    // Lazy rescale: P may exceed 1 by up to 2^kLazyRescale; O and l only get
+    // rescaled (here and in the O CTA) when the max grows beyond that.
+    float alpha = 1.f;
+    bool flag = false;
+    if (mt > m_used + kLazyRescale) {
+      alpha = ex2(m_used - mt);          // 0 when nothing was visible before
+      flag = (m_used != -CUDART_INF_F);  // an all-zero O row needs no rescale
+      m_used = mt;
+      l *= alpha;
+    }
+    const float msub = (m_used == -CUDART_INF_F) ? 0.f : m_used;
+    uint32_t hi[32], lo[32];
+    float lsum = 0.f;
+#pragma unroll
+    for (int c = 0; c < 32; ++c) {
+      const float p0 = ex2(y[2 * c] - msub);
+      const float p1 = ex2(y[2 * c + 1] - msub);
+      hi[c] = pack_bf16x2(p0, p1);
+      const float h0 = bf16lo_to_f32(hi[c]);
+      const float h1 = bf16hi_to_f32(hi[c]);
+      if (u.two_term) {
+        lo[c] = pack_bf16x2(p0 - h0, p1 - h1);
+        lsum += p0 + p1;
+      } else {
+        lsum += h0 + h1;
+      }
+    }
+    l += lsum;
+
+    // P buffer `buf` of the O CTA is free once its PV product of tile j-2 is done.
+    if (!wait_or_abort<true>(sm, smem_u32(&sm.pempty[buf]), ((j >> 1) & 1) ^ 1, p, 8)) return;
+    const uint32_t pfull_remote = buf ? pfull_remote1 : pfull_remote0;
+    const uint32_t dst_hi = p_remote + (2 * buf) * kPTerm + r * 128;
+#pragma unroll
+    for (int q4 = 0; q4 < 8; ++q4)
+      st_async_v4(dst_hi + ((q4 ^ (r & 7)) << 4),
+                  make_uint4(hi[4 * q4], hi[4 * q4 + 1], hi[4 * q4 + 2], hi[4 * q4 + 3]),
+                  pfull_remote);
+    if (u.two_term) {
+      const uint32_t dst_lo = dst_hi + kPTerm;
+#pragma unroll
+      for (int q4 = 0; q4 < 8; ++q4)
+        st_async_v4(dst_lo + ((q4 ^ (r & 7)) << 4),
+                    make_uint4(lo[4 * q4], lo[4 * q4 + 1], lo[4 * q4 + 2], lo[4 * q4 + 3]),
+                    pfull_remote);
+    }
+    st_async_b32(alpha_remote + (buf * kRows + r) * 4, __float_as_uint(alpha), pfull_remote);
+    const uint32_t any = __any_sync(0xFFFFFFFFu, flag) ? 1u : 0u;
+    if (lane == 0) st_async_b32(flags_remote + (buf * 4 + wq) * 4, any, pfull_remote);
+  }
+  st_async_v2(ml_remote + r * 8, __float_as_uint(m_used), __float_as_uint(l), mlfull_remote);
+}
+
+// ============================================================ O CTA roles
+
+__device__ __forceinline__ void o_producer(Smem& sm, const Unit& u, const SplitParams& p,
+                                           const CUtensorMap* map_kv, int& n_issued) {
+  const uint32_t ring = smem_u32(sm.ring);
+  for (int j = 0; j < u.ntiles; ++j) {
+    const int slot = j & 1;
+    if (!wait_or_abort(sm, smem_u32(&sm.vempty[slot]), ((j >> 1) & 1) ^ 1, p, 9)) return;
+    const uint32_t full = smem_u32(&sm.vfull[slot]);
+    mbar_arrive_expect_tx(full, kVTile);
+    for (int c = 0; c < kVChunks; ++c)
+      tma_load_3d(ring + slot * kVTile + c * kChunk, map_kv, 64 * c, u.k0 + j * kKeys, u.b, full);
+    n_issued = j + 1;
+  }
+}
+
+__device__ __forceinline__ uint32_t p_tile_bytes(const Unit& u) {
+  return (u.two_term ? 2u : 1u) * kPTerm + kRows * 4 + 4 * 4;
+}
+
+// Hand a command to the four O-CTA helper warps and wait until they are done.
+__device__ __forceinline__ bool o_command(Smem& sm, uint32_t cmd, int& ncmd,
+                                          const SplitParams& p) {
+  *reinterpret_cast<volatile uint32_t*>(&sm.cmd) = cmd;
+  mbar_arrive(smem_u32(&sm.corrgo));
+  const bool ok = wait_or_abort(sm, smem_u32(&sm.corrdone), ncmd & 1, p, 10);
+  ++ncmd;
+  return ok;
+}
+
+__device__ __forceinline__ void o_mma(Smem& sm, const Unit& u, const SplitParams& p,
+                                      uint32_t tmem) {
+  const uint32_t ring = smem_u32(sm.ring);
+  const uint32_t pbytes = p_tile_bytes(u);
+  int ncmd = 0;
+  bool ok = true;
+  for (int j = 0; j < u.ntiles && ok; ++j) {
+    const int buf = j & 1;
+    const int slot = j & 1;
+    if (!wait_or_abort<true>(sm, smem_u32(&sm.pfull[buf]), (j >> 1) & 1, p, 11)) { ok = false; break; }
+    if (j + 2 < u.ntiles) mbar_arrive_expect_tx(smem_u32(&sm.pfull[buf]), pbytes);
+    fence_proxy_async_smem();
+    if (!wait_or_abort(sm, smem_u32(&sm.vfull[slot]), (j >> 1) & 1, p, 12)) { ok = false; break; }
+    if (j == u.ntiles - 1 && u.zero_tail) {
+      if (!o_command(sm, kCmdZeroTail | static_cast<uint32_t>(j), ncmd, p)) { ok = false; break; }
+    }
+    const volatile uint32_t* fl = sm.flags[buf];
+    const bool flagged = j > 0 && (fl[0] | fl[1] | fl[2] | fl[3]) != 0;
+    if (flagged) {
+      // Rows whose max grew: O must be scaled after PV(j-1) lands and before
+      // PV(j) accumulates.  PV(j-2) is complete (its slot was refilled), so
+      // the only pending phase of vempty[(j-1)&1] is PV(j-1)'s.
+      if (!wait_or_abort(sm, smem_u32(&sm.vempty[(j - 1) & 1]), ((j - 1) >> 1) & 1, p, 13)) {
+        ok = false;
+        break;
+      }
+      if (!o_command(sm, static_cast<uint32_t>(j), ncmd, p)) { ok = false; break; }
+    }
+    tc_fence_after();
+    const uint32_t pb = ring + kPOffset + (2 * buf) * kPTerm;
+#pragma unroll
+    for (int ks = 0; ks < 4; ++ks) {
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const uint64_t adesc = sdesc_sw128(pb + ks * 32, 16, 1024);
+        const uint64_t bdesc =
+            sdesc_sw128(ring + slot * kVTile + 4 * h * kChunk + ks * 2048, kChunk, 1024);
+        mma_ss(tmem + 256 * h, adesc, bdesc, kIdescPV, (j > 0 || ks > 0) ? 1u : 0u);
+        if (u.two_term) {
+          const uint64_t adesc_lo = sdesc_sw128(pb + kPTerm + ks * 32, 16, 1024);
+          mma_ss(tmem + 256 * h, adesc_lo, bdesc, kIdescPV, 1u);
+        }
+      }
+    }
+    mma_commit(smem_u32(&sm.vempty[slot]));
+    mma_commit_mc(smem_u32(&sm.pempty[buf]), static_cast<uint16_t>(1u));  // rank 0 = S CTA
+  }
+  mma_commit(smem_u32(&sm.odone));
+  *reinterpret_cast<volatile uint32_t*>(&sm.cmd) = kCmdDone;
+  mbar_arrive(smem_u32(&sm.corrgo));
+}
+
+__device__ __forceinline__ void o_helpers(Smem& sm, const Unit& u, const SplitParams& p,
+                                          uint32_t tmem, int wq, int lane) {
+  const int r = wq * 32 + lane;
+  const uint32_t lane_base = static_cast<uint32_t>(wq * 32) << 16;
+  const int tid = wq * 32 + lane;
+  int ncmd = 0;
+  while (true) {
+    if (!wait_or_abort(sm, smem_u32(&sm.corrgo), ncmd & 1, p, 14)) return;
+    ++ncmd;
+    const uint32_t cmd = *reinterpret_cast<volatile uint32_t*>(&sm.cmd);
+    if (cmd == kCmdDone) break;
+    if (cmd & kCmdZeroTail) {
+      // Cache rows at or beyond the slice end hold arbitrary values (even NaN);
+      // P is 0 there but 0 * NaN would poison O, so clear them.
+      const int j = static_cast<int>(cmd & 0xFFFF);
+      const int z0 = u.k1 - (u.k0 + j * kKeys);
+      const int nrow = kKeys - z0;
+      uint8_t* tile = sm.ring + (j & 1) * kVTile;
+      for (int it = tid; it < nrow * kVChunks * 8; it += 128) {
+        const int q4 = it & 7;
+        const int rr = z0 + ((it >> 3) % nrow);
+        const int c = (it >> 3) / nrow;
+        *reinterpret_cast<uint4*>(tile + c * kChunk + rr * 128 + q4 * 16) = make_uint4(0, 0, 0, 0);
+      }
+      fence_proxy_async_smem();
+    } else {
+      const int buf = static_cast<int>(cmd) & 1;
+      const float a = sm.alpha[buf][r];
+      tc_fence_after();
+      if (__any_sync(0xFFFFFFFFu, a != 1.f)) {
+        for (int cc = 0; cc < 16; ++cc) {
+          uint32_t v[32];
+          MLA_TMEM_LD_32x32b_X32(tmem + lane_base + 32 * cc, v);
+          tmem_ld_wait();
+#pragma unroll
+          for (int e = 0; e < 32; ++e) v[e] = __float_as_uint(__uint_as_float(v[e]) * a);
+          MLA_TMEM_ST_32x32b_X32(tmem + lane_base + 32 * cc, v);
+        }
+        tmem_st_wait();
+      }
+      tc_fence_before();
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(smem_u32(&sm.corrdone));
+  }
+
+  // ---- epilogue
+  if (!wait_or_abort(sm, smem_u32(&sm.odone), 0, p, 15)) return;
+  if (!wait_or_abort<true>(sm, smem_u32(&sm.mlfull), 0, p, 16)) return;
+  tc_fence_after();
+  const float2 ml = sm.ml[r];
+  const bool valid = r < u.valid_rows;
+  const size_t grow = static_cast<size_t>(u.b) * u.rows_total + u.row0 + r;  // global row
+  const bool direct = p.nsplit == 1;
+  float* dst;
+  float scale_out = 1.f;
+  if (direct) {
+    dst = p.out + grow * kDl;
+    scale_out = ml.y > 0.f ? 1.f / ml.y : 0.f;
+  } else {
+    const size_t prow = static_cast<size_t>(u.sp) * p.B * u.rows_total + grow;
+    dst = p.part_o + prow * kDl;
+    if (valid) p.part_ml[prow] = ml;
+  }
+  for (int cc = 0; cc < 16; ++cc) {
+    uint32_t v[32];
+    MLA_TMEM_LD_32x32b_X32(tmem + lane_base + 32 * cc, v);
+    tmem_ld_wait();
+    if (valid) {
+      float4* d4 = reinterpret_cast<float4*>(dst + 32 * cc);
+#pragma unroll
+      for (int e = 0; e < 8; ++e)
+        d4[e] = make_float4(__uint_as_float(v[4 * e]) * scale_out,
+                            __uint_as_float(v[4 * e + 1]) * scale_out,
+                            __uint_as_float(v[4 * e + 2]) * scale_out,
+                            __uint_as_float(v[4 * e + 3]) * scale_out);
+    }
+  }
+  if (direct && valid)
+    p.lse[grow] = ml.y > 0.f ? (ml.x + log2f(ml.y)) * 0.6931471805599453f : -CUDART_INF_F;
+  tc_fence_before();
+}
+
+// ============================================================ kernel
+
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
+    verify_split_kernel(const __grid_constant__ CUtensorMap map_qn,
+                        const __grid_constant__ CUtensorMap map_qr,
+                        const __grid_constant__ CUtensorMap map_kv, const SplitParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  Smem& sm = *reinterpret_cast<Smem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                      ~static_cast<uintptr_t>(1023));
+  const int tid = threadIdx.x;
+  const int warp = tid >> 5;
+  const int lane = tid & 31;
+  const uint32_t role = cluster_ctarank();   // 0: scores + softmax, 1: PV accumulator
+  const Unit u = decode_unit(p);
+
+  if (tid == 0) {
+    if ((u.S < p.q || u.S > p.Smax) && role == 0 && u.sp == 0 && u.rt == 0)
+      atomicOr(p.status, kStatusSeqLen);
+    for (int i = 0; i < kKSlots; ++i) {
+      mbar_init(smem_u32(&sm.kfull[i]), 1);
+      mbar_init(smem_u32(&sm.kempty[i]), 1);
+    }
+    mbar_init(smem_u32(&sm.qfull), 1);
+    mbar_init(smem_u32(&sm.qready), 4);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(smem_u32(&sm.sfull[i]), 1);
+      mbar_init(smem_u32(&sm.sempty[i]), 4);
+      mbar_init(smem_u32(&sm.pempty[i]), 1);
+      mbar_init(smem_u32(&sm.pfull[i]), 1);
+      mbar_init(smem_u32(&sm.vfull[i]), 1);
+      mbar_init(smem_u32(&sm.vempty[i]), 1);
+    }
+    mbar_init(smem_u32(&sm.odone), 1);
+    mbar_init(smem_u32(&sm.corrgo), 1);
+    mbar_init(smem_u32(&sm.corrdone), 4);
+    mbar_init(smem_u32(&sm.mlfull), 1);
+    mbar_init(smem_u32(&sm.drain), 1);
+    sm.abort_flag = 0;
+    sm.cmd = 0;
+    if (role == 1 && !u.empty) {
+      // P buffers 0 and 1 expect tiles 0 and 1; m/l expect one pair per row.
+      mbar_arrive_expect_tx(smem_u32(&sm.pfull[0]), p_tile_bytes(u));
+      if (u.ntiles > 1) mbar_arrive_expect_tx(smem_u32(&sm.pfull[1]), p_tile_bytes(u));
+      mbar_arrive_expect_tx(smem_u32(&sm.mlfull), kRows * 8);
+    }
+    fence_mbarrier_init_cluster();
+  }
+  if (!u.empty && warp == 2) {
+    tmem_alloc(smem_u32(&sm.tmem_base), 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync_all();
+  tc_fence_after();
+  const uint32_t tmem = sm.tmem_base;
+
+  if (!u.empty) {
+    if (role == 0) {
+      if (warp == 0 && lane == 0) {
+        tma_prefetch_desc(&map_qn);
+        tma_prefetch_desc(&map_qr);
+        tma_prefetch_desc(&map_kv);
+        int n_issued = 0;
+        s_producer(sm, u, p, &map_qn, &map_qr, &map_kv, n_issued);
+        mbar_wait(smem_u32(&sm.qfull), 0, kWaitNs / 2);
+        drain_ring(sm.kfull, kKSlots, n_issued);
+      } else if (warp == 1 && lane == 0) {
+        s_mma(sm, u, p, tmem);
+        mma_commit(smem_u32(&sm.drain));
+        mbar_wait(smem_u32(&sm.drain), 0, kWaitNs);
+      } else if (warp >= 4) {
+        s_softmax(sm, u, p, tmem, warp - 4, lane);
+      }
+    } else {
+      if (warp == 0 && lane == 0) {
+        tma_prefetch_desc(&map_kv);
+        int n_issued = 0;
+        o_producer(sm, u, p, &map_kv, n_issued);
+        drain_ring(sm.vfull, kVSlots, n_issued);
+      } else if (warp == 1 && lane == 0) {
+        o_mma(sm, u, p, tmem);
+        mma_commit(smem_u32(&sm.drain));
+        mbar_wait(smem_u32(&sm.drain), 0, kWaitNs);
+      } else if (warp >= 4) {
+        o_helpers(sm, u, p, tmem, warp - 4, lane);
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (!u.empty && warp == 2) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+  cluster_sync_all();
+}
+
+}  // namespace mla

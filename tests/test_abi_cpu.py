@@ -1,0 +1,91 @@
+"""The C ABI without a GPU: the library builds, loads and exports every
+function the header declares; host-side argument checks return their codes
+before touching the device; the split planner's arithmetic."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import mla_verify_attention_gb300 as mva
+from mla_verify_attention_gb300 import _lib
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def header_functions():
+    names = []
+    for fn in os.listdir(os.path.join(ROOT, "include")):
+        if fn.endswith(".h"):
+            src = open(os.path.join(ROOT, "include", fn)).read()
+            src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+            names += re.findall(r"^\s*(?:const\s+)?[A-Za-z_][\w\s\*]*?\b(mla_\w+)\s*\(", src, re.M)
+    return sorted(set(names))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    return mva.load_library()
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = header_functions()
+    assert set(_lib.EXPORTED) <= set(names)
+    for n in names:
+        assert hasattr(lib, n), n
+
+
+def test_strerror(lib):
+    for code, name in _lib.STATUS_NAMES.items():
+        assert mva.strerror(code).startswith(name)
+    assert "unknown" in mva.strerror(12345)
+
+
+def call(lib, **kw):
+    a = dict(qn=16, qr=16, kv=16, sl=16, m=16, B=1, q=9, H=64, Smax=320, scale=0.07,
+             out=16, lse=16, ws=0, wsb=0)
+    a.update(kw)
+    return lib.mla_verify_attn(a["qn"], a["qr"], a["kv"], a["sl"], a["m"], a["B"], a["q"], a["H"],
+                               a["Smax"], a["scale"], a["out"], a["lse"], a["ws"], a["wsb"], None)
+
+
+def test_host_argument_checks(lib):
+    assert call(lib, q=0) == -2 and call(lib, q=65) == -2 and call(lib, H=0) == -2
+    assert call(lib, Smax=0) == -2 and call(lib, B=-1) == -2 and call(lib, Smax=1 << 24) == -2
+    assert call(lib, scale=float("nan")) == -9 and call(lib, scale=float("inf")) == -9
+    assert call(lib, B=0, qn=0, kv=0) == 0                      # nothing to do
+    for k in ("qn", "qr", "kv", "sl", "m", "out", "lse"):
+        assert call(lib, **{k: 0}) == -1, k
+    assert call(lib, kv=24) == -3 and call(lib, out=8) == -3 and call(lib, lse=2) == -3
+    assert call(lib, ws=272) == -3
+
+
+def test_no_device_is_reported(lib):
+    torch = pytest.importorskip("torch")
+    if torch.cuda.is_available():
+        pytest.skip("a device is present")
+    assert call(lib) == -5
+    assert lib.mla_verify_attn_workspace_size(1, 9, 64, 320) == 0
+
+
+def test_plan_arithmetic(lib):
+    # 152 SMs -> 76 two-CTA clusters.  One 64k stream of 9 drafts x 64 heads:
+    # 576 rows = 5 row tiles; 15 slices of 69 tiles fill 75 clusters.
+    assert mva.plan(1, 9, 64, 65600, 76) == (5, 15, 69)
+    # 33 drafts over 16k: 17 row tiles, 4 slices.
+    assert mva.plan(1, 33, 64, 16448, 76) == (17, 4, 65)
+    # short prefix: slices shorter than 8 tiles are not worth a cluster
+    assert mva.plan(1, 9, 64, 320, 76) == (5, 1, 5)
+    # ragged batch: smaller slices for balance
+    nrt, ns, ct = mva.plan(8, 9, 64, 32832, 76)
+    assert nrt == 5 and ns * ct >= 513 and (ns - 1) * ct < 513 and ct >= 8
+    # H other than 64 and one query row
+    assert mva.plan(1, 1, 1, 64, 76)[0] == 1
+    assert mva.plan(2, 3, 16, 1000, 76)[0] == 1
+
+
+def test_plan_env_override(lib, monkeypatch):
+    monkeypatch.setenv("MLA_VERIFY_NSPLIT", "3")
+    assert mva.plan(1, 9, 64, 320, 76) == (5, 3, 2)
+    monkeypatch.setenv("MLA_VERIFY_NSPLIT", "100")
+    assert mva.plan(1, 9, 64, 320, 76) == (5, 5, 1)

@@ -1,0 +1,178 @@
+"""CUDA path vs the fp64 oracle, through the C ABI, on seeded inputs.
+
+Tolerances (fixed for this path): max |out - oracle| <= 2e-3 and
+max |lse - oracle| <= 1e-3.  Cache rows past each stream's length are NaN in
+every case here and must have no influence.
+"""
+import os
+
+import numpy as np
+import pytest
+
+import oracle
+from mla_verify_attention_gb300 import inputs as I
+
+pytestmark = pytest.mark.gpu
+
+TOL_OUT = 2e-3
+TOL_LSE = 1e-3
+
+
+def to_dev(case):
+    import torch
+    dev = torch.device("cuda:0")
+
+    def t(a, dt):
+        return torch.from_numpy(np.ascontiguousarray(a)).view(dt).to(dev)
+
+    return (t(case.q_nope.view(np.int16), torch.bfloat16), t(case.q_rope.view(np.int16), torch.bfloat16),
+            t(case.kv.view(np.int16), torch.bfloat16), t(case.seq_lens, torch.int32),
+            t(case.mask.view(np.int32), torch.int32))
+
+
+def run_gpu(case, nsplit=None):
+    import torch
+    import mla_verify_attention_gb300 as mva
+    old = os.environ.get("MLA_VERIFY_NSPLIT")
+    if nsplit is not None:
+        os.environ["MLA_VERIFY_NSPLIT"] = str(nsplit)
+    try:
+        out, lse = mva.verify_attn(*to_dev(case), float(case.scale))
+        torch.cuda.synchronize()
+        st = mva.last_device_error()
+    finally:
+        if nsplit is not None:
+            if old is None:
+                os.environ.pop("MLA_VERIFY_NSPLIT", None)
+            else:
+                os.environ["MLA_VERIFY_NSPLIT"] = old
+    assert st == 0, mva.strerror(st)
+    return out.cpu().numpy().astype(np.float64), lse.cpu().numpy().astype(np.float64)
+
+
+def check(case, out, lse, rows=None):
+    ref_out, ref_lse = oracle.case_reference(case, rows=rows)
+    o = out.reshape(-1, 512)
+    l = lse.reshape(-1)
+    ro = ref_out.reshape(-1, 512)
+    rl = ref_lse.reshape(-1)
+    sel = slice(None) if rows is None else slice(rows[0], rows[0] + rows[1])
+    o, l, ro, rl = o[sel], l[sel], ro[sel], rl[sel]
+    empty = np.isneginf(rl)
+    assert np.array_equal(np.isneginf(l), empty), "empty-row pattern differs"
+    assert np.all(o[empty] == 0.0)
+    d_out = np.abs(o - ro).max()
+    d_lse = np.abs(l[~empty] - rl[~empty]).max() if (~empty).any() else 0.0
+    assert np.isfinite(o).all() and np.isfinite(l[~empty]).all()
+    assert d_out <= TOL_OUT and d_lse <= TOL_LSE, (d_out, d_lse)
+    return d_out, d_lse
+
+
+def custom_case(B, q, H, prefixes, seed, tree="random", max_depth=5, max_children=None,
+                smax_align=64):
+    w = I.Workload("custom", B, q, 0, tree, max_depth, max_children, H=H, index=0)
+    return I.make_case(w, seed=seed, prefixes=prefixes, smax_align=smax_align)
+
+
+# ---------------------------------------------------------------- small, full comparison
+
+def test_chain9_prefix256_full():
+    case = I.make_case(I.WORKLOADS["chain9_p256"])
+    check(case, *run_gpu(case))
+
+
+def test_tree9_prefix4096_full():
+    case = I.make_case(I.WORKLOADS["tree9_p4096"])
+    check(case, *run_gpu(case))
+
+
+@pytest.mark.parametrize("nsplit", [2, 3, 7])
+def test_forced_split_and_combine(nsplit):
+    case = custom_case(1, 9, 64, [1000], seed=101)
+    check(case, *run_gpu(case, nsplit=nsplit))
+
+
+@pytest.mark.parametrize("B,q,H,prefixes", [
+    (1, 1, 64, [0]),            # a single draft, no prefix: only itself
+    (1, 1, 64, [1]),            # one prefix key
+    (1, 9, 64, [0]),            # drafts only
+    (1, 9, 64, [55]),           # shorter than one key tile
+    (1, 9, 64, [63]),           # slice ends one short of a tile
+    (1, 9, 64, [119]),          # seq_len = 128: exactly two tiles
+    (1, 32, 64, [300]),         # full first mask word
+    (1, 33, 64, [200]),         # second mask word, half row tile
+    (2, 64, 64, [70, 5]),       # widest draft count
+    (1, 9, 16, [500]),          # fewer heads (row tile spans drafts)
+    (3, 5, 8, [10, 200, 65]),   # ragged, tiny row count
+    (1, 2, 128, [90]),          # more heads than a row tile
+])
+def test_edge_shapes(B, q, H, prefixes):
+    case = custom_case(B, q, H, prefixes, seed=7 + q + H + sum(prefixes))
+    check(case, *run_gpu(case))
+
+
+def test_edge_shapes_split():
+    case = custom_case(3, 5, 8, [10, 900, 2000], seed=77)
+    check(case, *run_gpu(case, nsplit=4))
+
+
+def test_empty_rows_are_zero_and_minus_inf():
+    case = custom_case(1, 4, 64, [0], seed=9, tree="chain")
+    case.mask[0, 0, 0] = 0          # draft 0 sees nothing at all
+    out, lse = run_gpu(case)
+    check(case, out, lse)
+    assert np.all(np.isneginf(lse[0, 0]))
+
+
+def test_growing_scores_exercise_rescale():
+    # Later keys score ever higher, so the running max keeps growing past the
+    # lazy-rescale margin and the O rows must be rescaled in tensor memory.
+    case = custom_case(1, 9, 64, [2000], seed=55)
+    kv = I.bf16_bits_to_f32(case.kv).copy()
+    S = case.seq_lens[0]
+    ramp = np.linspace(0.2, 3.0, S, dtype=np.float32)[:, None]
+    kv[0, :S] *= ramp
+    case.kv = I.f32_to_bf16_bits(kv)
+    case.kv[0, S:] = 0x7FC0
+    check(case, *run_gpu(case))
+    check(case, *run_gpu(case, nsplit=3))
+
+
+def test_masked_draft_rows_have_no_influence():
+    case = custom_case(1, 9, 64, [300], seed=31)
+    out0, lse0 = run_gpu(case)
+    P = case.seq_lens[0] - 9
+    hidden = [j for j in range(9) if all(not (case.mask[0, i, 0] >> j) & 1 for i in range(9))]
+    # every draft sees itself in an ancestor tree, so make one draft invisible
+    case.mask[0, :, 0] &= ~np.uint32(1 << 8)
+    out1, lse1 = run_gpu(case)
+    case.kv[0, P + 8] = I.f32_to_bf16_bits(np.full(576, 1e3, np.float32))
+    out2, lse2 = run_gpu(case)
+    np.testing.assert_array_equal(out1, out2)
+    np.testing.assert_array_equal(lse1, lse2)
+    assert not hidden
+
+
+def test_deterministic():
+    case = custom_case(1, 9, 64, [3000], seed=5)
+    a = run_gpu(case)
+    b = run_gpu(case)
+    np.testing.assert_array_equal(a[0], b[0])
+    np.testing.assert_array_equal(a[1], b[1])
+
+
+# ---------------------------------------------------------------- full-size workloads
+
+def sampled_rows(case, n=3):
+    rows = case.B * case.q * case.H
+    starts = np.linspace(0, rows - 64, n).astype(int)
+    return [(int(s), 64) for s in starts]
+
+
+@pytest.mark.parametrize("name", ["tree33_p16384", "tree9_p65536", "ragged8_tree9"])
+def test_full_size_sampled(name):
+    case = I.make_case(I.WORKLOADS[name])
+    out, lse = run_gpu(case)
+    assert np.isfinite(out).all() and np.isfinite(lse).all()
+    for rows in sampled_rows(case):
+        check(case, out, lse, rows=rows)
