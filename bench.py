@@ -1,0 +1,423 @@
+#!/usr/bin/env python
+"""Benchmark of the absorbed-MLA verify-attention call on GB300.
+
+One step = one verify call (split kernel + slice merge) over one synthetic
+workload; default workload: 1 stream, 9 draft-tree queries x 64 heads over a
+65536-token latent prefix (576-wide bf16 cache rows).  Prints ONE JSON line.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Timing: W untimed calls, then exactly K calls bracketed by a barrier and
+torch.cuda.synchronize() on both sides, timed with CUDA events on the stream
+the kernels run on.  The cache is rotated over enough copies that the working
+set exceeds L2, so every call reads its cache cold from HBM.  SM clocks and
+throttle reasons are sampled with nvidia-smi during the timed region.
+
+--impl reference times the fp64 CPU oracle (the only other implementation of
+this computation) on the host cores, on a bounded sample of the same workload.
+With N > 1 (torchrun), every rank runs its own replica of the workload (the
+path has no cross-GPU exchange; "replicas only"); the reported time is the
+maximum over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from mla_verify_attention_gb300 import inputs as I  # noqa: E402
+
+METRIC = "verify-attn us/call (q_len=9, prefix 65536)"
+UNIT = "us/call"
+PAGES_US = {"tree9_p65536": 19722.2}   # best sm_120 time the pages report for this workload
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="tree9_p65536", choices=sorted(I.WORKLOADS))
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-budget-s", type=float, default=20.0)
+    ap.add_argument("--e2e-steps", type=int, default=20)
+    return ap.parse_args()
+
+
+# ----------------------------------------------------------------------- helpers
+
+def work_of(case):
+    """Algorithmic FLOPs and cache bytes of one call (cache read once)."""
+    rows = case.q * case.H
+    keys = int(np.sum(case.seq_lens.astype(np.int64)))
+    flops = 2.0 * rows * keys * (512 + 64 + 512)
+    cache_bytes = keys * 576 * 2
+    return flops, cache_bytes
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as fh:
+            m = json.load(fh)
+        return float(m["hbm_gbs"]), float(m["bf16_tflops"]), "measured"
+    except Exception:
+        return 6800.0, 1900.0, "fallback"
+
+
+def kernel_src_hash():
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "mla_verify_attention_gb300", "csrc")
+    for fn in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, fn), "rb") as fh:
+            h.update(fn.encode() + fh.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(workload):
+    """DRAM bytes per call from the committed ncu summary, if it is current."""
+    path = os.path.join(ROOT, "profiles", "traffic_%s.json" % workload)
+    try:
+        with open(path) as fh:
+            t = json.load(fh)
+    except Exception:
+        return None
+    if t.get("kernel_src_sha256_16") != kernel_src_hash():
+        return None
+    return t.get("dram_bytes_per_call")
+
+
+class ClockSampler:
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(prefix="clocks_", suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), "--query-gpu=" + self.FIELDS,
+                 "--format=csv,noheader,nounits", "-lms", "20"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except Exception:
+            self.proc = None
+
+    def stop(self, window=None):
+        """Summarise the samples whose timestamps fall inside `window`
+        (host wall-clock seconds); all samples if none do."""
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        import datetime
+        rows, inside = [], []
+        with open(self.path) as fh:
+            for line in fh:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) >= 10:
+                    try:
+                        ts = datetime.datetime.strptime(parts[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+                    except ValueError:
+                        ts = None
+                    rows.append(parts[1:])
+                    if window and ts is not None and window[0] <= ts <= window[1]:
+                        inside.append(parts[1:])
+        os.unlink(self.path)
+        in_window = bool(inside)
+        if inside:
+            rows = inside
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+
+        sm = [num(r[1]) for r in rows if num(r[1]) is not None]
+        smax = [num(r[2]) for r in rows if num(r[2]) is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[k] for r in rows for k in range(4) if r[5 + k].lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": reasons, "samples": len(rows), "in_timed_window": in_window,
+                "power_w_max": max((num(r[3]) or 0.0) for r in rows)}
+
+
+def physical_gpu_index(local_rank):
+    vis = os.environ.get("CUDA_VISIBLE_DEVICES")
+    if vis:
+        ids = [v.strip() for v in vis.split(",") if v.strip()]
+        if local_rank < len(ids) and ids[local_rank].isdigit():
+            return int(ids[local_rank])
+    return local_rank
+
+
+def oracle_sample(case, budget_s, steps=1):
+    """Time the oracle on whole calls if they fit the budget, else on a row
+    sample; returns (us per full call, cores, sample description)."""
+    import oracle
+    rows = case.B * case.q * case.H
+    cores = os.cpu_count() or 1
+    n0 = min(rows, max(8, cores))
+    t0 = time.perf_counter()
+    oracle.case_reference(case, nthreads=cores, rows=(0, n0))
+    per_row = (time.perf_counter() - t0) / n0
+    n = rows if per_row * rows <= budget_s else max(n0, int(budget_s / per_row))
+    n = min(rows, n)
+    times = []
+    for s in range(steps):
+        start = (s * n) % rows if n < rows else 0
+        cnt = min(n, rows - start)
+        t0 = time.perf_counter()
+        oracle.case_reference(case, nthreads=cores, rows=(start, cnt))
+        times.append((time.perf_counter() - t0) * rows / cnt)
+    us = statistics.median(times) * 1e6
+    what = ("whole call (%d query rows)" % rows if n >= rows else
+            "%d of %d query rows per step, scaled to the whole call" % (n, rows))
+    return us, cores, what, times
+
+
+# ----------------------------------------------------------------------- arms
+
+def run_reference(args, rank):
+    if rank != 0:
+        return
+    case = I.make_case(I.WORKLOADS[args.workload], pad="normal")
+    # each step is a bounded sample so that the whole run ends within minutes
+    budget = min(args.cpu_budget_s, 120.0 / max(1, args.steps + 1))
+    for _ in range(max(0, min(args.warmup, 1))):
+        oracle_sample(case, budget / 4)
+    us, cores, what, times = oracle_sample(case, budget, steps=args.steps)
+    line = {
+        "impl": "reference", "metric": METRIC, "value": us, "unit": UNIT, "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": us / 1e3,
+        "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": config_of(args.workload, case),
+        "cpu_baseline": {"value": us, "unit": UNIT, "cores": cores, "kind": "oracle",
+                         "sample": what},
+        "e2e": {"value": us, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+    print(json.dumps(line), flush=True)
+
+
+def config_of(name, case, extra=None):
+    w = I.WORKLOADS[name]
+    c = {"workload": name, "B": case.B, "q_len": case.q, "H": case.H, "Dl": 512, "Dr": 64,
+         "prefix": w.prefix if not isinstance(w.prefix, tuple) else list(w.prefix),
+         "seq_lens": [int(s) for s in case.seq_lens], "Smax": case.Smax,
+         "tree": "chain" if w.tree == "chain" else
+                 "random, depth<=%d%s" % (w.max_depth, "" if w.max_children is None
+                                          else ", branching<=%d" % w.max_children),
+         "inputs": "bf16 N(0,1) from seed %#x" % w.seed, "scale": "1/sqrt(192)"}
+    if extra:
+        c.update(extra)
+    return c
+
+
+def run_ours(args, rank, world, local_rank):
+    import torch
+    import mla_verify_attention_gb300 as mva
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    mva.load_library()
+    case = I.make_case(I.WORKLOADS[args.workload], pad="normal")
+
+    def t(a, dt):
+        return torch.from_numpy(np.ascontiguousarray(a)).view(dt).to(dev)
+
+    q_nope = t(case.q_nope.view(np.int16), torch.bfloat16)
+    q_rope = t(case.q_rope.view(np.int16), torch.bfloat16)
+    seq = t(case.seq_lens, torch.int32)
+    mask = t(case.mask.view(np.int32), torch.int32)
+    kv0 = t(case.kv.view(np.int16), torch.bfloat16)
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    kv_bytes = kv0.numel() * 2
+    copies = max(2, math.ceil(2.0 * l2 / kv_bytes) + 1)
+    kvs = [kv0] + [kv0.clone() for _ in range(copies - 1)]
+    B, q, H, Smax = case.B, case.q, case.H, case.Smax
+    out = torch.empty((B, q, H, 512), dtype=torch.float32, device=dev)
+    lse = torch.empty((B, q, H), dtype=torch.float32, device=dev)
+    need = mva.workspace_size(B, q, H, Smax)
+    ws = torch.empty(max(need, 1), dtype=torch.uint8, device=dev)
+    n_rt, nsplit, chunk = mva.plan(B, q, H, Smax)
+    launches_per_call = 1 + (1 if nsplit > 1 else 0)
+    stream = torch.cuda.current_stream(dev)
+    sh = int(stream.cuda_stream)
+    ptrs = [q_nope.data_ptr(), q_rope.data_ptr(), None, seq.data_ptr(), mask.data_ptr()]
+
+    def call(i):
+        st = mva.verify_attn_raw(ptrs[0], ptrs[1], kvs[i % copies].data_ptr(), ptrs[3], ptrs[4], B,
+                                 q, H, Smax, float(case.scale), out.data_ptr(), lse.data_ptr(),
+                                 ws.data_ptr(), ws.numel(), sh)
+        if st != 0:
+            raise mva.MLAError(st)
+
+    dist = world > 1
+    if dist:
+        import torch.distributed as tdist
+    for i in range(max(3, args.warmup)):
+        call(i)
+    torch.cuda.synchronize(dev)
+    st = mva.last_device_error()
+    if st != 0:
+        raise mva.MLAError(st, "warm-up")
+
+    sampler = ClockSampler(physical_gpu_index(local_rank))
+    sampler.start()
+    ev0 = torch.cuda.Event(enable_timing=True)
+    ev1 = torch.cuda.Event(enable_timing=True)
+    if dist:
+        tdist.barrier()
+    torch.cuda.synchronize(dev)
+    t_wall0 = time.time()
+    ev0.record(stream)
+    for i in range(args.steps):
+        call(i)
+    ev1.record(stream)
+    torch.cuda.synchronize(dev)
+    t_wall1 = time.time()
+    if dist:
+        tdist.barrier()
+    clocks = sampler.stop(window=(t_wall0, t_wall1))
+    ms = ev0.elapsed_time(ev1)
+    us_call = ms * 1e3 / args.steps
+    if dist:
+        v = torch.tensor([us_call], device=dev)
+        tdist.all_reduce(v, op=tdist.ReduceOp.MAX)
+        us_call = float(v.item())
+    st = mva.last_device_error()
+    if st != 0:
+        raise mva.MLAError(st, "timed region")
+
+    # ---- end to end through the public API, from pinned host buffers
+    host_in = [torch.from_numpy(np.ascontiguousarray(a)).pin_memory() for a in
+               (case.q_nope.view(np.int16), case.q_rope.view(np.int16), case.kv.view(np.int16),
+                case.seq_lens, case.mask.view(np.int32))]
+    h_out = torch.empty((B, q, H, 512), dtype=torch.float32).pin_memory()
+    h_lse = torch.empty((B, q, H), dtype=torch.float32).pin_memory()
+    d_in = [torch.empty(h.shape, dtype=h.dtype, device=dev) for h in host_in]
+    h2d = sum(h.numel() * h.element_size() for h in host_in)
+    d2h = h_out.numel() * 4 + h_lse.numel() * 4
+
+    def e2e_step():
+        for d, h in zip(d_in, host_in):
+            d.copy_(h, non_blocking=True)
+        o, l = mva.verify_attn(d_in[0].view(torch.bfloat16), d_in[1].view(torch.bfloat16),
+                               d_in[2].view(torch.bfloat16), d_in[3], d_in[4], float(case.scale),
+                               out=out, lse=lse, workspace=ws if need > 0 else None)
+        h_out.copy_(o, non_blocking=True)
+        h_lse.copy_(l, non_blocking=True)
+
+    for _ in range(3):
+        e2e_step()
+    torch.cuda.synchronize(dev)
+    n_e2e = max(1, args.e2e_steps)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(n_e2e):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    e2e_us = e0.elapsed_time(e1) * 1e3 / n_e2e
+
+    flops, cache_bytes = work_of(case)
+    hbm_gbs, bf16_tf, peak_src = measured_peaks()
+    t_tensor = flops / (bf16_tf * 1e12)
+    t_hbm = cache_bytes / (hbm_gbs * 1e9)
+    if t_tensor >= t_hbm:
+        achieved = flops / (us_call * 1e-6) / 1e12
+        roof = {"bound": "tensor", "achieved": achieved, "peak": bf16_tf, "unit": "TFLOP/s",
+                "frac": achieved / bf16_tf}
+    else:
+        achieved = cache_bytes / (us_call * 1e-6) / 1e9
+        roof = {"bound": "hbm", "achieved": achieved, "peak": hbm_gbs, "unit": "GB/s",
+                "frac": achieved / hbm_gbs}
+    roof["traffic"] = recorded_traffic(args.workload)
+    roof["peak_source"] = "%s (MEASURED_PEAKS.json burst)" % peak_src if peak_src == "measured" \
+        else "fallback"
+    roof["kernel"] = "whole verify call: split kernel + slice merge (%d launch%s)" % (
+        launches_per_call, "es" if launches_per_call > 1 else "")
+    roof["algorithmic"] = {"flops_per_call": flops, "cache_bytes_per_call": cache_bytes}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        c_us, cores, what, _ = oracle_sample(case, args.cpu_budget_s)
+        cpu = {"value": c_us, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": what}
+
+    if rank == 0:
+        ref = PAGES_US.get(args.workload)
+        line = {
+            "metric": METRIC if args.workload == "tree9_p65536" else
+            "verify-attn us/call (%s)" % args.workload,
+            "value": us_call, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": max(3, args.warmup), "ms_per_step": us_call / 1e3,
+            "higher_is_better": False, "scaling": "weak",
+            "vs_baseline": (us_call / ref) if ref else None,
+            "dtype": "bf16", "data": "synthetic",
+            "config": config_of(args.workload, case, {
+                "l2": "inputs larger than L2: %d rotating cache copies (%.0f MB > %.0f MB L2)" % (
+                    copies, copies * kv_bytes / 1e6, l2 / 1e6),
+                "plan": {"row_tiles": n_rt, "nsplit": nsplit, "chunk_tiles": chunk},
+                "parallelism": "replicas" if world > 1 else "single GPU",
+                "vs_baseline_ref": ("pages' best sm_120 time for this workload: %.1f us "
+                                    "(RTX PRO 6000, fp32), context only" % ref) if ref else None}),
+            "roofline": roof,
+            "cpu_baseline": cpu,
+            "e2e": {"value": e2e_us, "unit": UNIT, "h2d_bytes_per_step": h2d,
+                    "d2h_bytes_per_step": d2h},
+            "gpu_launches": args.steps * launches_per_call,
+            "clocks": clocks,
+        }
+        print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse()
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        run_reference(args, rank)
+        return
+    if world > 1:
+        import torch
+        import torch.distributed as tdist
+        torch.cuda.set_device(local_rank)
+        tdist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+    try:
+        run_ours(args, rank, world, local_rank)
+    finally:
+        if world > 1:
+            import torch.distributed as tdist
+            tdist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -35,10 +35,12 @@ __global__ void __launch_bounds__(128) combine_kernel(const CombineParams p) {
   const int S = p.seq_lens[b];
   if (S < p.q || S > p.Smax) return;   // reported by the split kernel
   const int ns = min(p.nsplit, (S + p.chunk_keys - 1) / p.chunk_keys);
+  const float2* ml = p.part_ml + row;
   float M = -CUDART_INF_F;
+#pragma unroll 8
   for (int s = 0; s < ns; ++s) {
-    const float2 ml = p.part_ml[static_cast<size_t>(s) * p.N + row];
-    if (ml.y > 0.f) M = fmaxf(M, ml.x);
+    const float2 v = ml[static_cast<size_t>(s) * p.N];
+    M = v.y > 0.f ? fmaxf(M, v.x) : M;
   }
   float4* dst = reinterpret_cast<float4*>(p.out + static_cast<size_t>(row) * 512) + tid;
   if (M == -CUDART_INF_F) {
@@ -46,19 +48,23 @@ __global__ void __launch_bounds__(128) combine_kernel(const CombineParams p) {
     if (tid == 0) p.lse[row] = -CUDART_INF_F;
     return;
   }
+  // Slices with l = 0 hold an all-zero accumulator: weight 0, nothing to read.
   float L = 0.f;
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  const float4* src = reinterpret_cast<const float4*>(p.part_o + static_cast<size_t>(row) * 512) + tid;
+  const size_t step4 = static_cast<size_t>(p.N) * 128;   // float4s between slices
+#pragma unroll 4
   for (int s = 0; s < ns; ++s) {
-    const size_t idx = static_cast<size_t>(s) * p.N + row;
-    const float2 ml = p.part_ml[idx];
-    if (!(ml.y > 0.f)) continue;
-    const float w = ex2(ml.x - M);
-    L += w * ml.y;
-    const float4 o = reinterpret_cast<const float4*>(p.part_o + idx * 512)[tid];
-    acc.x += w * o.x;
-    acc.y += w * o.y;
-    acc.z += w * o.z;
-    acc.w += w * o.w;
+    const float2 v = ml[static_cast<size_t>(s) * p.N];
+    const float w = v.y > 0.f ? ex2(v.x - M) : 0.f;
+    L += w * v.y;
+    if (w != 0.f) {
+      const float4 o = src[s * step4];
+      acc.x += w * o.x;
+      acc.y += w * o.y;
+      acc.z += w * o.z;
+      acc.w += w * o.w;
+    }
   }
   const float inv = 1.f / L;
   *dst = make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);

@@ -138,7 +138,7 @@ bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p
 
 int encode(DeviceInfo* d, CUtensorMap* map, const void* base, int rank, const cuuint64_t* dims,
            const cuuint64_t* strides, const cuuint32_t* box) {
-  const cuuint32_t elem[3] = {1, 1, 1};
+  const cuuint32_t elem[4] = {1, 1, 1, 1};
   const CUresult r = d->encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, const_cast<void*>(base),
                                dims, strides, box, elem, CU_TENSOR_MAP_INTERLEAVE_NONE,
                                CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -212,12 +212,16 @@ int mla_verify_attn(const void* q_nope_abs, const void* q_rope, const void* kv,
   if (need > 0 && (!workspace || workspace_bytes < need)) return MLA_ERR_WORKSPACE;
 
   const long long rows = static_cast<long long>(B) * q_len * H;
-  CUtensorMap map_qn, map_qr, map_kv;
+  // Tensor maps.  Each cache (and q_nope) row of 576 (512) bf16 is viewed as
+  // chunks of 64 dims; the chunk index is its own dimension (stride 128 B) so
+  // that one TMA box brings [chunk][row][64 dims] into shared memory, i.e. a
+  // whole 64-key tile per copy, in the 128-byte-swizzled layout the MMAs read.
+  CUtensorMap map_qn, map_qr, map_kvs, map_kvo;
   {
-    const cuuint64_t dims[2] = {512, static_cast<cuuint64_t>(rows)};
-    const cuuint64_t strides[1] = {512 * 2};
-    const cuuint32_t box[2] = {64, mla::kRows};
-    if (encode(d, &map_qn, q_nope_abs, 2, dims, strides, box) != MLA_OK) return MLA_ERR_LAUNCH;
+    const cuuint64_t dims[3] = {64, static_cast<cuuint64_t>(rows), 8};
+    const cuuint64_t strides[2] = {512 * 2, 64 * 2};
+    const cuuint32_t box[3] = {64, mla::kRows, 8};
+    if (encode(d, &map_qn, q_nope_abs, 3, dims, strides, box) != MLA_OK) return MLA_ERR_LAUNCH;
   }
   {
     const cuuint64_t dims[2] = {64, static_cast<cuuint64_t>(rows)};
@@ -226,10 +230,12 @@ int mla_verify_attn(const void* q_nope_abs, const void* q_rope, const void* kv,
     if (encode(d, &map_qr, q_rope, 2, dims, strides, box) != MLA_OK) return MLA_ERR_LAUNCH;
   }
   {
-    const cuuint64_t dims[3] = {576, static_cast<cuuint64_t>(Smax), static_cast<cuuint64_t>(B)};
-    const cuuint64_t strides[2] = {576 * 2, static_cast<cuuint64_t>(Smax) * 576 * 2};
-    const cuuint32_t box[3] = {64, mla::kKeys, 1};
-    if (encode(d, &map_kv, kv, 3, dims, strides, box) != MLA_OK) return MLA_ERR_LAUNCH;
+    const cuuint64_t dims[4] = {64, static_cast<cuuint64_t>(Smax), 9, static_cast<cuuint64_t>(B)};
+    const cuuint64_t strides[3] = {576 * 2, 64 * 2, static_cast<cuuint64_t>(Smax) * 576 * 2};
+    const cuuint32_t box_s[4] = {64, mla::kKeys, 9, 1};
+    const cuuint32_t box_o[4] = {64, mla::kKeys, 8, 1};
+    if (encode(d, &map_kvs, kv, 4, dims, strides, box_s) != MLA_OK) return MLA_ERR_LAUNCH;
+    if (encode(d, &map_kvo, kv, 4, dims, strides, box_o) != MLA_OK) return MLA_ERR_LAUNCH;
   }
 
   mla::SplitParams p;
@@ -255,7 +261,7 @@ int mla_verify_attn(const void* q_nope_abs, const void* q_rope, const void* kv,
   const long long units = static_cast<long long>(B) * nrt * ns;
   if (2 * units >= (1LL << 31)) return MLA_ERR_SHAPE;
   mla::verify_split_kernel<<<static_cast<unsigned>(2 * units), mla::kThreads, kSmemBytes, stream>>>(
-      map_qn, map_qr, map_kv, p);
+      map_qn, map_qr, map_kvs, map_kvo, p);
   if (cudaGetLastError() != cudaSuccess) return MLA_ERR_LAUNCH;
   if (ns > 1) {
     mla::CombineParams c;

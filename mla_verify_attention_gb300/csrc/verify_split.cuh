@@ -51,13 +51,20 @@ constexpr int kChunk = kKeys * 64 * 2;           // 8 KB: 64 keys x 64 dims bf16
 constexpr int kQChunk = kRows * 64 * 2;          // 16 KB: 128 rows x 64 dims bf16
 constexpr int kKChunks = 9;                      // 576 / 64
 constexpr int kVChunks = 8;                      // 512 / 64
-constexpr int kKSlots = 24;                      // S CTA key-chunk ring
-constexpr int kVSlots = 2;                       // O CTA value-tile ring
-constexpr int kVTile = kVChunks * kChunk;        // 64 KB
-constexpr int kPTerm = kRows * kKeys * 2;        // 16 KB per P term buffer
+constexpr int kKSlots = 2;                       // S CTA key-tile ring: 2 x 72 KB
+constexpr int kVSlots = 2;                       // O CTA value-tile ring: 2 x 64 KB
+constexpr int kKTile = kKChunks * kChunk;        // 72 KB: one TMA box per tile
+constexpr int kVTile = kVChunks * kChunk;        // 64 KB: one TMA box per tile
+constexpr int kPTerm = kRows * kKeys * 2;        // 16 KB per P term
+// One P exchange buffer: [alpha: 128 f32 | flags: 4 u32 | pad][P hi][P lo].
+// The S CTA fills its copy and moves it with one bulk copy into the same
+// offset of the O CTA, where the PV MMA reads P from it.
+constexpr int kPHead = 1024;
+constexpr int kPBuf = kPHead + 2 * kPTerm;
+constexpr int kPOffset = kKSlots * kKTile;       // after the K ring / V tiles (144 KB)
 constexpr int kThreads = 256;
-constexpr int kRingBytes = 192 * 1024;
-constexpr int kPOffset = kVSlots * kVTile;       // P buffers follow the two V tiles
+constexpr int kRingBytes = kPOffset + 2 * kPBuf;
+constexpr uint32_t kSoftmaxBar = 1;              // named barrier of the 4 softmax warps
 constexpr uint32_t kQCols = 288;                 // Q in tensor memory: 576 bf16 = 288 cols
 constexpr float kLazyRescale = 8.0f;             // log2 units: keep the max unless it grows by 2^8
 constexpr uint64_t kWaitNs = 2000000000ull;      // bounded waits: 2 s
@@ -86,8 +93,6 @@ struct SplitParams {
 
 struct __align__(1024) Smem {
   uint8_t ring[kRingBytes];
-  float alpha[2][kRows];
-  uint32_t flags[2][4];
   float2 ml[kRows];
   uint64_t kfull[kKSlots], kempty[kKSlots];
   uint64_t qfull, qready;
@@ -159,6 +164,15 @@ __device__ __forceinline__ bool wait_or_abort(Smem& sm, uint32_t bar, uint32_t p
   return wait_slow<kCluster>(sm, bar, parity, p, site);
 }
 
+// Wait by a whole converged warp; the result is made warp-uniform so that the
+// warp can keep executing .sync.aligned / elect.sync instructions together.
+template <bool kCluster = false>
+__device__ __forceinline__ bool warp_wait(Smem& sm, uint32_t bar, uint32_t parity,
+                                          const SplitParams& p, int site) {
+  const bool ok = wait_or_abort<kCluster>(sm, bar, parity, p, site);
+  return __all_sync(0xFFFFFFFFu, ok);
+}
+
 // Before a CTA exits, every TMA copy it issued must have landed: wait for the
 // last phase each ring slot was armed for.  Consumed phases return at once.
 __device__ __forceinline__ void drain_ring(const uint64_t* full, int nslots, int n_issued) {
@@ -174,52 +188,51 @@ __device__ __forceinline__ void s_producer(Smem& sm, const Unit& u, const SplitP
   const uint32_t ring = smem_u32(sm.ring);
   const uint32_t qfull = smem_u32(&sm.qfull);
   // Q rows of this unit: 8 latent chunks + 1 rope chunk of [128 rows x 64 dims].
+  // Two boxes: [8 chunks][128 rows][64 dims] of q_nope and [128 rows][64] of q_rope.
   const int y = u.b * u.rows_total + u.row0;
   mbar_arrive_expect_tx(qfull, kKChunks * kQChunk);
-  for (int c = 0; c < kVChunks; ++c) tma_load_2d(ring + c * kQChunk, map_qn, 64 * c, y, qfull);
+  tma_load_3d(ring, map_qn, 0, y, 0, qfull);
   tma_load_2d(ring + kVChunks * kQChunk, map_qr, 0, y, qfull);
   // The Q staging area overlaps the first ring slots: wait until the softmax
   // warps have moved Q into tensor memory.
   if (!wait_or_abort(sm, smem_u32(&sm.qready), 0, p, 1)) return;
   fence_proxy_async();
-  int n = 0;
+  // One box per 64-key tile: [9 chunks][64 keys][64 dims].
   for (int j = 0; j < u.ntiles; ++j) {
-    const int key = u.k0 + j * kKeys;
-    for (int c = 0; c < kKChunks; ++c, ++n) {
-      const int slot = n % kKSlots;
-      const uint32_t ph = (n / kKSlots) & 1;
-      if (!wait_or_abort(sm, smem_u32(&sm.kempty[slot]), ph ^ 1, p, 2)) return;
-      const uint32_t full = smem_u32(&sm.kfull[slot]);
-      mbar_arrive_expect_tx(full, kChunk);
-      tma_load_3d(ring + slot * kChunk, map_kv, 64 * c, key, u.b, full);
-      n_issued = n + 1;
-    }
+    const int slot = j % kKSlots;
+    if (!wait_or_abort(sm, smem_u32(&sm.kempty[slot]), ((j / kKSlots) & 1) ^ 1, p, 2)) return;
+    const uint32_t full = smem_u32(&sm.kfull[slot]);
+    mbar_arrive_expect_tx(full, kKTile);
+    tma_load_4d(ring + slot * kKTile, map_kv, 0, u.k0 + j * kKeys, 0, u.b, full);
+    n_issued = j + 1;
   }
 }
 
+// The MMA warp runs converged; one elected lane issues (issue cost then stays
+// negligible next to the 36 MMAs of a tile).
 __device__ __forceinline__ void s_mma(Smem& sm, const Unit& u, const SplitParams& p,
                                       uint32_t tmem) {
   const uint32_t ring = smem_u32(sm.ring);
-  if (!wait_or_abort(sm, smem_u32(&sm.qready), 0, p, 3)) return;
+  if (!warp_wait(sm, smem_u32(&sm.qready), 0, p, 3)) return;
   tc_fence_after();
-  int n = 0;
   for (int j = 0; j < u.ntiles; ++j) {
     const int buf = j & 1;
-    if (!wait_or_abort(sm, smem_u32(&sm.sempty[buf]), ((j >> 1) & 1) ^ 1, p, 4)) return;
+    if (!warp_wait(sm, smem_u32(&sm.sempty[buf]), ((j >> 1) & 1) ^ 1, p, 4)) return;
     tc_fence_after();
     const uint32_t d = tmem + kQCols + 64 * buf;
-    for (int c = 0; c < kKChunks; ++c, ++n) {
-      const int slot = n % kKSlots;
-      if (!wait_or_abort(sm, smem_u32(&sm.kfull[slot]), (n / kKSlots) & 1, p, 5)) return;
-      tc_fence_after();
+    const int slot = j % kKSlots;
+    if (!warp_wait(sm, smem_u32(&sm.kfull[slot]), (j / kKSlots) & 1, p, 5)) return;
+    tc_fence_after();
 #pragma unroll
-      for (int ks = 0; ks < 4; ++ks) {
-        const uint64_t bdesc = sdesc_sw128(ring + slot * kChunk + ks * 32, 16, 1024);
-        mma_ts(d, tmem + c * 32 + ks * 8, bdesc, kIdescQK, (c | ks) != 0);
-      }
-      mma_commit(smem_u32(&sm.kempty[slot]));
+    for (int c = 0; c < kKChunks; ++c) {
+      const uint32_t kb = ring + slot * kKTile + c * kChunk;
+#pragma unroll
+      for (int ks = 0; ks < 4; ++ks)
+        mma_ts_elect(d, tmem + c * 32 + ks * 8, sdesc_sw128(kb + ks * 32, 16, 1024), kIdescQK,
+                     (c | ks) != 0);
     }
-    mma_commit(smem_u32(&sm.sfull[buf]));
+    mma_commit_elect(smem_u32(&sm.kempty[slot]));
+    mma_commit_elect(smem_u32(&sm.sfull[buf]));
   }
 }
 
@@ -239,8 +252,10 @@ __device__ __forceinline__ void s_softmax(Smem& sm, const Unit& u, const SplitPa
     if (p.q < 64) mask64 &= (1ull << p.q) - 1ull;
   }
 
-  // ---- Q: staging shared memory -> registers -> tensor memory
-  if (!wait_or_abort(sm, smem_u32(&sm.qfull), 0, p, 6)) return;
+  // ---- Q: staging shared memory -> registers -> tensor memory.  All exits of
+  // the four softmax warps are taken together (they share named barriers).
+  const bool qok = warp_wait(sm, smem_u32(&sm.qfull), 0, p, 6);
+  if (named_bar_red_or(kSoftmaxBar, 128, !qok)) return;
   for (int c = 0; c < kKChunks; ++c) {
     const uint8_t* src = sm.ring + c * kQChunk + r * 128;
     uint32_t v[32];
@@ -259,23 +274,29 @@ __device__ __forceinline__ void s_softmax(Smem& sm, const Unit& u, const SplitPa
   __syncwarp();
   if (lane == 0) mbar_arrive(smem_u32(&sm.qready));
 
-  // ---- peer (O CTA) addresses
+  // ---- peer (O CTA) addresses: the exchange buffers sit at the same offsets
   const uint32_t peer = 1;
-  const uint32_t p_remote = mapa_shared(smem_u32(sm.ring + kPOffset), peer);
-  const uint32_t alpha_remote = mapa_shared(smem_u32(&sm.alpha[0][0]), peer);
-  const uint32_t flags_remote = mapa_shared(smem_u32(&sm.flags[0][0]), peer);
+  const uint32_t xbuf0 = smem_u32(sm.ring + kPOffset);
+  const uint32_t xbuf0_remote = mapa_shared(xbuf0, peer);
   const uint32_t pfull_remote0 = mapa_shared(smem_u32(&sm.pfull[0]), peer);
   const uint32_t pfull_remote1 = mapa_shared(smem_u32(&sm.pfull[1]), peer);
   const uint32_t ml_remote = mapa_shared(smem_u32(&sm.ml[0]), peer);
   const uint32_t mlfull_remote = mapa_shared(smem_u32(&sm.mlfull), peer);
+  const uint32_t xbytes = kPHead + (u.two_term ? 2u : 1u) * kPTerm;
 
-  const float sl2 = p.scale_log2;
+  const float a = p.scale_log2;
   float m_used = -CUDART_INF_F;   // log2-scaled running max actually used for P
-  float l = 0.f;                  // running sum of P (as fed to the PV product)
+  float l = 0.f;                  // running sum of P
 
+  bool copy_failed = false;       // set by the copy-issuing thread only
+  bool finished = true;
   for (int j = 0; j < u.ntiles; ++j) {
     const int buf = j & 1;
-    if (!wait_or_abort(sm, smem_u32(&sm.sfull[buf]), (j >> 1) & 1, p, 7)) return;
+    const bool got = warp_wait(sm, smem_u32(&sm.sfull[buf]), (j >> 1) & 1, p, 7);
+    if (named_bar_red_or(kSoftmaxBar, 128, !got || copy_failed)) {
+      finished = false;
+      break;
+    }
     tc_fence_after();
     uint32_t sr[64];
     MLA_TMEM_LD_32x32b_X32(tmem + lane_base + kQCols + 64 * buf, sr);
@@ -285,75 +306,98 @@ __device__ __forceinline__ void s_softmax(Smem& sm, const Unit& u, const SplitPa
     __syncwarp();
     if (lane == 0) mbar_arrive(smem_u32(&sm.sempty[buf]));
 
+    // Scaled scores y = s * scale * log2(e); masked keys get -inf.  Keys of a
+    // tile that lies wholly inside the prefix are all visible; otherwise bit c
+    // of `vis` says whether key key0+c is visible to this row.
     const int key0 = u.k0 + j * kKeys;
-    float y[64];
-    const bool all_visible = row_valid && (key0 + kKeys <= u.prefix);
-    if (all_visible) {
-#pragma unroll
-      for (int c = 0; c < 64; ++c) y[c] = __uint_as_float(sr[c]) * sl2;
-    } else {
-#pragma unroll
-      for (int c = 0; c < 64; ++c) {
-        const int t = key0 + c;
-        bool vis = row_valid && (t < u.S);
-        if (vis && t >= u.prefix) vis = (mask64 >> (t - u.prefix)) & 1ull;
-        y[c] = vis ? __uint_as_float(sr[c]) * sl2 : -CUDART_INF_F;
-      }
-    }
-    float mt = y[0];
-#pragma unroll
-    for (int c = 1; c < 64; ++c) mt = fmaxf(mt, y[c]);
-    // Lazy rescale: P may exceed 1 by up to 2^kLazyRescale; O and l only get
-    // rescaled (here and in the O CTA) when the max grows beyond that.
     float alpha = 1.f;
     bool flag = false;
-    if (mt > m_used + kLazyRescale) {
-      alpha = ex2(m_used - mt);          // 0 when nothing was visible before
-      flag = (m_used != -CUDART_INF_F);  // an all-zero O row needs no rescale
-      m_used = mt;
-      l *= alpha;
-    }
-    const float msub = (m_used == -CUDART_INF_F) ? 0.f : m_used;
     uint32_t hi[32], lo[32];
-    float lsum = 0.f;
+    if (row_valid) {
+      if (key0 + kKeys <= u.prefix) {
 #pragma unroll
-    for (int c = 0; c < 32; ++c) {
-      const float p0 = ex2(y[2 * c] - msub);
-      const float p1 = ex2(y[2 * c + 1] - msub);
-      hi[c] = pack_bf16x2(p0, p1);
-      const float h0 = bf16lo_to_f32(hi[c]);
-      const float h1 = bf16hi_to_f32(hi[c]);
-      if (u.two_term) {
-        lo[c] = pack_bf16x2(p0 - h0, p1 - h1);
-        lsum += p0 + p1;
+        for (int c = 0; c < 64; ++c) sr[c] = __float_as_uint(__uint_as_float(sr[c]) * a);
       } else {
-        lsum += h0 + h1;
+        const int np = u.prefix - key0;             // prefix keys in this tile (may be <= 0)
+        uint64_t vis = np >= 64 ? ~0ull : (np > 0 ? (1ull << np) - 1ull : 0ull);
+        uint64_t drafts = mask64;                   // bit j: draft j visible
+        if (np > 0) drafts = np >= 64 ? 0ull : drafts << np;
+        else drafts = drafts >> (-np);              // -np < q <= 64
+        vis |= drafts;
+        const int nk = u.S - key0;                  // keys of the stream in this tile
+        if (nk < 64) vis &= nk > 0 ? (1ull << nk) - 1ull : 0ull;
+#pragma unroll
+        for (int c = 0; c < 64; ++c)
+          sr[c] = ((vis >> c) & 1ull) ? __float_as_uint(__uint_as_float(sr[c]) * a)
+                                      : __float_as_uint(-CUDART_INF_F);
       }
+      float mx[8];
+#pragma unroll
+      for (int k = 0; k < 8; ++k) mx[k] = __uint_as_float(sr[k]);
+#pragma unroll
+      for (int c = 8; c < 64; ++c) mx[c & 7] = fmaxf(mx[c & 7], __uint_as_float(sr[c]));
+      const float mt = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
+                             fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
+      // Lazy rescale: P may exceed 1 by up to 2^kLazyRescale; O and l only get
+      // rescaled (here and in the O CTA) when the max grows beyond that.
+      if (mt > m_used + kLazyRescale) {
+        alpha = ex2(m_used - mt);          // 0 when nothing was visible before
+        flag = (m_used != -CUDART_INF_F);  // an all-zero O row needs no rescale
+        m_used = mt;
+        l *= alpha;
+      }
+      const float msub = (m_used == -CUDART_INF_F) ? 0.f : m_used;
+      float ls[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+      for (int c = 0; c < 32; ++c) {
+        const float p0 = ex2(__uint_as_float(sr[2 * c]) - msub);
+        const float p1 = ex2(__uint_as_float(sr[2 * c + 1]) - msub);
+        ls[c & 3] += p0 + p1;
+        hi[c] = pack_bf16x2(p0, p1);
+        if (u.two_term) lo[c] = pack_bf16x2(p0 - bf16lo_to_f32(hi[c]), p1 - bf16hi_to_f32(hi[c]));
+      }
+      l += (ls[0] + ls[1]) + (ls[2] + ls[3]);
+    } else {
+      // Rows past the stream's q*H rows (the tail of the last row tile): P = 0.
+#pragma unroll
+      for (int c = 0; c < 32; ++c) hi[c] = lo[c] = 0u;
     }
-    l += lsum;
 
-    // P buffer `buf` of the O CTA is free once its PV product of tile j-2 is done.
-    if (!wait_or_abort<true>(sm, smem_u32(&sm.pempty[buf]), ((j >> 1) & 1) ^ 1, p, 8)) return;
-    const uint32_t pfull_remote = buf ? pfull_remote1 : pfull_remote0;
-    const uint32_t dst_hi = p_remote + (2 * buf) * kPTerm + r * 128;
+    // Stage [alpha | flags | P hi | P lo] locally, then one bulk copy into the
+    // O CTA.  The copy that last read this buffer (tile j-2) was waited for by
+    // its issuer before the barrier at the top of this iteration.
+    uint8_t* xb = sm.ring + kPOffset + buf * kPBuf;
+    reinterpret_cast<float*>(xb)[r] = alpha;
+    const uint32_t any = __any_sync(0xFFFFFFFFu, flag) ? 1u : 0u;
+    if (lane == 0) reinterpret_cast<uint32_t*>(xb + 512)[wq] = any;
+    uint8_t* ph = xb + kPHead + r * 128;
 #pragma unroll
     for (int q4 = 0; q4 < 8; ++q4)
-      st_async_v4(dst_hi + ((q4 ^ (r & 7)) << 4),
-                  make_uint4(hi[4 * q4], hi[4 * q4 + 1], hi[4 * q4 + 2], hi[4 * q4 + 3]),
-                  pfull_remote);
+      *reinterpret_cast<uint4*>(ph + ((q4 ^ (r & 7)) << 4)) =
+          make_uint4(hi[4 * q4], hi[4 * q4 + 1], hi[4 * q4 + 2], hi[4 * q4 + 3]);
     if (u.two_term) {
-      const uint32_t dst_lo = dst_hi + kPTerm;
 #pragma unroll
       for (int q4 = 0; q4 < 8; ++q4)
-        st_async_v4(dst_lo + ((q4 ^ (r & 7)) << 4),
-                    make_uint4(lo[4 * q4], lo[4 * q4 + 1], lo[4 * q4 + 2], lo[4 * q4 + 3]),
-                    pfull_remote);
+        *reinterpret_cast<uint4*>(ph + kPTerm + ((q4 ^ (r & 7)) << 4)) =
+            make_uint4(lo[4 * q4], lo[4 * q4 + 1], lo[4 * q4 + 2], lo[4 * q4 + 3]);
     }
-    st_async_b32(alpha_remote + (buf * kRows + r) * 4, __float_as_uint(alpha), pfull_remote);
-    const uint32_t any = __any_sync(0xFFFFFFFFu, flag) ? 1u : 0u;
-    if (lane == 0) st_async_b32(flags_remote + (buf * 4 + wq) * 4, any, pfull_remote);
+    fence_proxy_async_smem();
+    named_bar_sync(kSoftmaxBar, 128);
+    if (r == 0) {
+      // The O CTA's buffer `buf` is free once its PV product of tile j-2 is done.
+      if (wait_or_abort<true>(sm, smem_u32(&sm.pempty[buf]), ((j >> 1) & 1) ^ 1, p, 8)) {
+        bulk_copy_to_peer(xbuf0_remote + buf * kPBuf, xbuf0 + buf * kPBuf, xbytes,
+                          buf ? pfull_remote1 : pfull_remote0);
+        bulk_commit_group();
+        bulk_wait_read<1>();
+      } else {
+        copy_failed = true;
+      }
+    }
   }
-  st_async_v2(ml_remote + r * 8, __float_as_uint(m_used), __float_as_uint(l), mlfull_remote);
+  if (r == 0) bulk_wait_read<0>();
+  if (finished && !named_bar_red_or(kSoftmaxBar, 128, copy_failed))
+    st_async_v2(ml_remote + r * 8, __float_as_uint(m_used), __float_as_uint(l), mlfull_remote);
 }
 
 // ============================================================ O CTA roles
@@ -366,76 +410,78 @@ __device__ __forceinline__ void o_producer(Smem& sm, const Unit& u, const SplitP
     if (!wait_or_abort(sm, smem_u32(&sm.vempty[slot]), ((j >> 1) & 1) ^ 1, p, 9)) return;
     const uint32_t full = smem_u32(&sm.vfull[slot]);
     mbar_arrive_expect_tx(full, kVTile);
-    for (int c = 0; c < kVChunks; ++c)
-      tma_load_3d(ring + slot * kVTile + c * kChunk, map_kv, 64 * c, u.k0 + j * kKeys, u.b, full);
+    tma_load_4d(ring + slot * kVTile, map_kv, 0, u.k0 + j * kKeys, 0, u.b, full);
     n_issued = j + 1;
   }
 }
 
 __device__ __forceinline__ uint32_t p_tile_bytes(const Unit& u) {
-  return (u.two_term ? 2u : 1u) * kPTerm + kRows * 4 + 4 * 4;
+  return kPHead + (u.two_term ? 2u : 1u) * kPTerm;
 }
 
 // Hand a command to the four O-CTA helper warps and wait until they are done.
-__device__ __forceinline__ bool o_command(Smem& sm, uint32_t cmd, int& ncmd,
-                                          const SplitParams& p) {
-  *reinterpret_cast<volatile uint32_t*>(&sm.cmd) = cmd;
-  mbar_arrive(smem_u32(&sm.corrgo));
-  const bool ok = wait_or_abort(sm, smem_u32(&sm.corrdone), ncmd & 1, p, 10);
+// Called by the whole MMA warp.
+__device__ __forceinline__ bool o_command(Smem& sm, uint32_t cmd, int& ncmd, const SplitParams& p,
+                                          int lane) {
+  if (lane == 0) {
+    *reinterpret_cast<volatile uint32_t*>(&sm.cmd) = cmd;
+    mbar_arrive(smem_u32(&sm.corrgo));
+  }
+  __syncwarp();
+  const bool ok = warp_wait(sm, smem_u32(&sm.corrdone), ncmd & 1, p, 10);
   ++ncmd;
   return ok;
 }
 
 __device__ __forceinline__ void o_mma(Smem& sm, const Unit& u, const SplitParams& p,
-                                      uint32_t tmem) {
+                                      uint32_t tmem, int lane) {
   const uint32_t ring = smem_u32(sm.ring);
   const uint32_t pbytes = p_tile_bytes(u);
   int ncmd = 0;
-  bool ok = true;
-  for (int j = 0; j < u.ntiles && ok; ++j) {
+  for (int j = 0; j < u.ntiles; ++j) {
     const int buf = j & 1;
     const int slot = j & 1;
-    if (!wait_or_abort<true>(sm, smem_u32(&sm.pfull[buf]), (j >> 1) & 1, p, 11)) { ok = false; break; }
-    if (j + 2 < u.ntiles) mbar_arrive_expect_tx(smem_u32(&sm.pfull[buf]), pbytes);
+    if (!warp_wait<true>(sm, smem_u32(&sm.pfull[buf]), (j >> 1) & 1, p, 11)) break;
+    if (lane == 0 && j + 2 < u.ntiles) mbar_arrive_expect_tx(smem_u32(&sm.pfull[buf]), pbytes);
     fence_proxy_async_smem();
-    if (!wait_or_abort(sm, smem_u32(&sm.vfull[slot]), (j >> 1) & 1, p, 12)) { ok = false; break; }
+    if (!warp_wait(sm, smem_u32(&sm.vfull[slot]), (j >> 1) & 1, p, 12)) break;
     if (j == u.ntiles - 1 && u.zero_tail) {
-      if (!o_command(sm, kCmdZeroTail | static_cast<uint32_t>(j), ncmd, p)) { ok = false; break; }
+      if (!o_command(sm, kCmdZeroTail | static_cast<uint32_t>(j), ncmd, p, lane)) break;
     }
-    const volatile uint32_t* fl = sm.flags[buf];
+    const uint8_t* xb = sm.ring + kPOffset + buf * kPBuf;
+    const volatile uint32_t* fl = reinterpret_cast<const volatile uint32_t*>(xb + 512);
     const bool flagged = j > 0 && (fl[0] | fl[1] | fl[2] | fl[3]) != 0;
     if (flagged) {
       // Rows whose max grew: O must be scaled after PV(j-1) lands and before
       // PV(j) accumulates.  PV(j-2) is complete (its slot was refilled), so
       // the only pending phase of vempty[(j-1)&1] is PV(j-1)'s.
-      if (!wait_or_abort(sm, smem_u32(&sm.vempty[(j - 1) & 1]), ((j - 1) >> 1) & 1, p, 13)) {
-        ok = false;
-        break;
-      }
-      if (!o_command(sm, static_cast<uint32_t>(j), ncmd, p)) { ok = false; break; }
+      if (!warp_wait(sm, smem_u32(&sm.vempty[(j - 1) & 1]), ((j - 1) >> 1) & 1, p, 13)) break;
+      if (!o_command(sm, static_cast<uint32_t>(j), ncmd, p, lane)) break;
     }
     tc_fence_after();
-    const uint32_t pb = ring + kPOffset + (2 * buf) * kPTerm;
+    const uint32_t pb = ring + kPOffset + buf * kPBuf + kPHead;
+    const uint32_t vb = ring + slot * kVTile;
 #pragma unroll
     for (int ks = 0; ks < 4; ++ks) {
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
-        const uint64_t adesc = sdesc_sw128(pb + ks * 32, 16, 1024);
-        const uint64_t bdesc =
-            sdesc_sw128(ring + slot * kVTile + 4 * h * kChunk + ks * 2048, kChunk, 1024);
-        mma_ss(tmem + 256 * h, adesc, bdesc, kIdescPV, (j > 0 || ks > 0) ? 1u : 0u);
-        if (u.two_term) {
-          const uint64_t adesc_lo = sdesc_sw128(pb + kPTerm + ks * 32, 16, 1024);
-          mma_ss(tmem + 256 * h, adesc_lo, bdesc, kIdescPV, 1u);
-        }
+        const uint64_t bdesc = sdesc_sw128(vb + 4 * h * kChunk + ks * 2048, kChunk, 1024);
+        mma_ss_elect(tmem + 256 * h, sdesc_sw128(pb + ks * 32, 16, 1024), bdesc, kIdescPV,
+                     (j > 0 || ks > 0) ? 1u : 0u);
+        if (u.two_term)
+          mma_ss_elect(tmem + 256 * h, sdesc_sw128(pb + kPTerm + ks * 32, 16, 1024), bdesc,
+                       kIdescPV, 1u);
       }
     }
-    mma_commit(smem_u32(&sm.vempty[slot]));
-    mma_commit_mc(smem_u32(&sm.pempty[buf]), static_cast<uint16_t>(1u));  // rank 0 = S CTA
+    mma_commit_elect(smem_u32(&sm.vempty[slot]));
+    mma_commit_mc_elect(smem_u32(&sm.pempty[buf]), static_cast<uint16_t>(1u));  // rank 0 = S CTA
   }
-  mma_commit(smem_u32(&sm.odone));
-  *reinterpret_cast<volatile uint32_t*>(&sm.cmd) = kCmdDone;
-  mbar_arrive(smem_u32(&sm.corrgo));
+  mma_commit_elect(smem_u32(&sm.odone));
+  if (lane == 0) {
+    *reinterpret_cast<volatile uint32_t*>(&sm.cmd) = kCmdDone;
+    mbar_arrive(smem_u32(&sm.corrgo));
+  }
+  __syncwarp();
 }
 
 __device__ __forceinline__ void o_helpers(Smem& sm, const Unit& u, const SplitParams& p,
@@ -445,7 +491,7 @@ __device__ __forceinline__ void o_helpers(Smem& sm, const Unit& u, const SplitPa
   const int tid = wq * 32 + lane;
   int ncmd = 0;
   while (true) {
-    if (!wait_or_abort(sm, smem_u32(&sm.corrgo), ncmd & 1, p, 14)) return;
+    if (!warp_wait(sm, smem_u32(&sm.corrgo), ncmd & 1, p, 14)) return;
     ++ncmd;
     const uint32_t cmd = *reinterpret_cast<volatile uint32_t*>(&sm.cmd);
     if (cmd == kCmdDone) break;
@@ -465,15 +511,15 @@ __device__ __forceinline__ void o_helpers(Smem& sm, const Unit& u, const SplitPa
       fence_proxy_async_smem();
     } else {
       const int buf = static_cast<int>(cmd) & 1;
-      const float a = sm.alpha[buf][r];
+      const float alpha = reinterpret_cast<const float*>(sm.ring + kPOffset + buf * kPBuf)[r];
       tc_fence_after();
-      if (__any_sync(0xFFFFFFFFu, a != 1.f)) {
+      if (__any_sync(0xFFFFFFFFu, alpha != 1.f)) {
         for (int cc = 0; cc < 16; ++cc) {
           uint32_t v[32];
           MLA_TMEM_LD_32x32b_X32(tmem + lane_base + 32 * cc, v);
           tmem_ld_wait();
 #pragma unroll
-          for (int e = 0; e < 32; ++e) v[e] = __float_as_uint(__uint_as_float(v[e]) * a);
+          for (int e = 0; e < 32; ++e) v[e] = __float_as_uint(__uint_as_float(v[e]) * alpha);
           MLA_TMEM_ST_32x32b_X32(tmem + lane_base + 32 * cc, v);
         }
         tmem_st_wait();
@@ -485,8 +531,8 @@ __device__ __forceinline__ void o_helpers(Smem& sm, const Unit& u, const SplitPa
   }
 
   // ---- epilogue
-  if (!wait_or_abort(sm, smem_u32(&sm.odone), 0, p, 15)) return;
-  if (!wait_or_abort<true>(sm, smem_u32(&sm.mlfull), 0, p, 16)) return;
+  if (!warp_wait(sm, smem_u32(&sm.odone), 0, p, 15)) return;
+  if (!warp_wait<true>(sm, smem_u32(&sm.mlfull), 0, p, 16)) return;
   tc_fence_after();
   const float2 ml = sm.ml[r];
   const bool valid = r < u.valid_rows;
@@ -526,7 +572,8 @@ __device__ __forceinline__ void o_helpers(Smem& sm, const Unit& u, const SplitPa
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     verify_split_kernel(const __grid_constant__ CUtensorMap map_qn,
                         const __grid_constant__ CUtensorMap map_qr,
-                        const __grid_constant__ CUtensorMap map_kv, const SplitParams p) {
+                        const __grid_constant__ CUtensorMap map_kvs,
+                        const __grid_constant__ CUtensorMap map_kvo, const SplitParams p) {
   extern __shared__ uint8_t smem_raw[];
   Smem& sm = *reinterpret_cast<Smem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                       ~static_cast<uintptr_t>(1023));
@@ -583,28 +630,30 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       if (warp == 0 && lane == 0) {
         tma_prefetch_desc(&map_qn);
         tma_prefetch_desc(&map_qr);
-        tma_prefetch_desc(&map_kv);
+        tma_prefetch_desc(&map_kvs);
         int n_issued = 0;
-        s_producer(sm, u, p, &map_qn, &map_qr, &map_kv, n_issued);
+        s_producer(sm, u, p, &map_qn, &map_qr, &map_kvs, n_issued);
         mbar_wait(smem_u32(&sm.qfull), 0, kWaitNs / 2);
         drain_ring(sm.kfull, kKSlots, n_issued);
-      } else if (warp == 1 && lane == 0) {
+      } else if (warp == 1) {
         s_mma(sm, u, p, tmem);
-        mma_commit(smem_u32(&sm.drain));
+        mma_commit_elect(smem_u32(&sm.drain));
         mbar_wait(smem_u32(&sm.drain), 0, kWaitNs);
+        __syncwarp();
       } else if (warp >= 4) {
         s_softmax(sm, u, p, tmem, warp - 4, lane);
       }
     } else {
       if (warp == 0 && lane == 0) {
-        tma_prefetch_desc(&map_kv);
+        tma_prefetch_desc(&map_kvo);
         int n_issued = 0;
-        o_producer(sm, u, p, &map_kv, n_issued);
+        o_producer(sm, u, p, &map_kvo, n_issued);
         drain_ring(sm.vfull, kVSlots, n_issued);
-      } else if (warp == 1 && lane == 0) {
-        o_mma(sm, u, p, tmem);
-        mma_commit(smem_u32(&sm.drain));
+      } else if (warp == 1) {
+        o_mma(sm, u, p, tmem, lane);
+        mma_commit_elect(smem_u32(&sm.drain));
         mbar_wait(smem_u32(&sm.drain), 0, kWaitNs);
+        __syncwarp();
       } else if (warp >= 4) {
         o_helpers(sm, u, p, tmem, warp - 4, lane);
       }
