@@ -48,22 +48,30 @@ __global__ void __launch_bounds__(128) combine_kernel(const CombineParams p) {
     if (tid == 0) p.lse[row] = -CUDART_INF_F;
     return;
   }
-  // Slices with l = 0 hold an all-zero accumulator: weight 0, nothing to read.
+  // Every slice s < ns wrote its partial (an all-zero accumulator where no key
+  // was visible), so the loads are unconditional: eight independent 16-byte
+  // loads are in flight per thread.
   float L = 0.f;
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
   const float4* src = reinterpret_cast<const float4*>(p.part_o + static_cast<size_t>(row) * 512) + tid;
   const size_t step4 = static_cast<size_t>(p.N) * 128;   // float4s between slices
-#pragma unroll 4
-  for (int s = 0; s < ns; ++s) {
-    const float2 v = ml[static_cast<size_t>(s) * p.N];
-    const float w = v.y > 0.f ? ex2(v.x - M) : 0.f;
-    L += w * v.y;
-    if (w != 0.f) {
-      const float4 o = src[s * step4];
-      acc.x += w * o.x;
-      acc.y += w * o.y;
-      acc.z += w * o.z;
-      acc.w += w * o.w;
+  for (int s0 = 0; s0 < ns; s0 += 8) {
+    float4 o[8];
+    float w[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      const int s = min(s0 + e, ns - 1);
+      o[e] = src[s * step4];
+      const float2 v = ml[static_cast<size_t>(s) * p.N];
+      w[e] = (s0 + e < ns && v.y > 0.f) ? ex2(v.x - M) : 0.f;
+      L += w[e] * (s0 + e < ns ? v.y : 0.f);
+    }
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      acc.x += w[e] * o[e].x;
+      acc.y += w[e] * o[e].y;
+      acc.z += w[e] * o[e].z;
+      acc.w += w[e] * o[e].w;
     }
   }
   const float inv = 1.f / L;

@@ -269,6 +269,25 @@ __device__ __forceinline__ void mma_ts_elect(uint32_t d_tmem, uint32_t a_tmem, u
       : "memory");
 }
 
+// Four MMAs along K (one 64-wide bf16 chunk = 4 x K16 steps) issued by one
+// elected lane.  A in tensor memory advances 8 columns per step; the B
+// descriptor's start address advances 32 bytes (2 descriptor units) per step.
+// `accumulate` applies to the first MMA only; the other three accumulate.
+__device__ __forceinline__ void mma_ts_chunk_elect(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                                   uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred e, p;\n .reg .b32 a1, a2, a3;\n .reg .b64 b1, b2, b3;\n"
+      " elect.sync _|e, 0xffffffff;\n setp.ne.b32 p, %4, 0;\n"
+      " add.u32 a1, %1, 8;\n add.u32 a2, %1, 16;\n add.u32 a3, %1, 24;\n"
+      " add.s64 b1, %2, 2;\n add.s64 b2, %2, 4;\n add.s64 b3, %2, 6;\n"
+      " @e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n"
+      " @e tcgen05.mma.cta_group::1.kind::f16 [%0], [a1], b1, %3, 1;\n"
+      " @e tcgen05.mma.cta_group::1.kind::f16 [%0], [a2], b2, %3, 1;\n"
+      " @e tcgen05.mma.cta_group::1.kind::f16 [%0], [a3], b3, %3, 1;\n}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
 // Commit by the elected lane (the lane that issued the MMAs above).
 __device__ __forceinline__ void mma_commit_elect(uint32_t bar) {
   asm volatile(

@@ -62,9 +62,10 @@ constexpr int kPTerm = kRows * kKeys * 2;        // 16 KB per P term
 constexpr int kPHead = 1024;
 constexpr int kPBuf = kPHead + 2 * kPTerm;
 constexpr int kPOffset = kKSlots * kKTile;       // after the K ring / V tiles (144 KB)
-constexpr int kThreads = 256;
+constexpr int kThreads = 384;                    // 12 warps: 4 control + 8 row warps
 constexpr int kRingBytes = kPOffset + 2 * kPBuf;
-constexpr uint32_t kSoftmaxBar = 1;              // named barrier of the 4 softmax warps
+constexpr uint32_t kSoftmaxBar = 1;              // named barrier of the 8 softmax warps
+constexpr int kRowThreads = 256;                 // two threads per row (one per 32-key half)
 constexpr uint32_t kQCols = 288;                 // Q in tensor memory: 576 bf16 = 288 cols
 constexpr float kLazyRescale = 8.0f;             // log2 units: keep the max unless it grows by 2^8
 constexpr uint64_t kWaitNs = 2000000000ull;      // bounded waits: 2 s
@@ -94,6 +95,8 @@ struct SplitParams {
 struct __align__(1024) Smem {
   uint8_t ring[kRingBytes];
   float2 ml[kRows];
+  float xmax[2][kRows];      // S CTA: per-half partial row max of the current tile
+  float xl[kRows];           // S CTA: second half's running sum, combined at the end
   uint64_t kfull[kKSlots], kempty[kKSlots];
   uint64_t qfull, qready;
   uint64_t sfull[2], sempty[2];
@@ -223,21 +226,23 @@ __device__ __forceinline__ void s_mma(Smem& sm, const Unit& u, const SplitParams
     const int slot = j % kKSlots;
     if (!warp_wait(sm, smem_u32(&sm.kfull[slot]), (j / kKSlots) & 1, p, 5)) return;
     tc_fence_after();
+    // Descriptor of chunk c = descriptor of chunk 0 + c * 8 KB (in 16-byte units).
+    const uint64_t bdesc0 = sdesc_sw128(ring + slot * kKTile, 16, 1024);
 #pragma unroll
-    for (int c = 0; c < kKChunks; ++c) {
-      const uint32_t kb = ring + slot * kKTile + c * kChunk;
-#pragma unroll
-      for (int ks = 0; ks < 4; ++ks)
-        mma_ts_elect(d, tmem + c * 32 + ks * 8, sdesc_sw128(kb + ks * 32, 16, 1024), kIdescQK,
-                     (c | ks) != 0);
-    }
+    for (int c = 0; c < kKChunks; ++c)
+      mma_ts_chunk_elect(d, tmem + c * 32, bdesc0 + static_cast<uint64_t>(c * (kChunk >> 4)),
+                         kIdescQK, c != 0);
     mma_commit_elect(smem_u32(&sm.kempty[slot]));
     mma_commit_elect(smem_u32(&sm.sfull[buf]));
   }
 }
 
+// Eight softmax warps: warp 4+w and warp 8+w both own tensor-memory lanes
+// 32w..32w+31 (one query row per lane); the first takes keys 0..31 of each
+// tile, the second keys 32..63.  The two halves agree on the row max through
+// shared memory once per tile; each keeps its own part of the running sum.
 __device__ __forceinline__ void s_softmax(Smem& sm, const Unit& u, const SplitParams& p,
-                                          uint32_t tmem, int wq, int lane) {
+                                          uint32_t tmem, int wq, int half, int lane) {
   const int r = wq * 32 + lane;                     // row of the unit == tensor-memory lane
   const uint32_t lane_base = static_cast<uint32_t>(wq * 32) << 16;
   const int R = u.row0 + r;
@@ -252,11 +257,12 @@ __device__ __forceinline__ void s_softmax(Smem& sm, const Unit& u, const SplitPa
     if (p.q < 64) mask64 &= (1ull << p.q) - 1ull;
   }
 
-  // ---- Q: staging shared memory -> registers -> tensor memory.  All exits of
-  // the four softmax warps are taken together (they share named barriers).
+  // ---- Q: staging shared memory -> registers -> tensor memory (each half
+  // moves four or five of the nine 64-dim chunks of its row).  All exits of
+  // the softmax warps are taken together (they share named barriers).
   const bool qok = warp_wait(sm, smem_u32(&sm.qfull), 0, p, 6);
-  if (named_bar_red_or(kSoftmaxBar, 128, !qok)) return;
-  for (int c = 0; c < kKChunks; ++c) {
+  if (named_bar_red_or(kSoftmaxBar, kRowThreads, !qok)) return;
+  for (int c = half; c < kKChunks; c += 2) {
     const uint8_t* src = sm.ring + c * kQChunk + r * 128;
     uint32_t v[32];
 #pragma unroll
@@ -280,110 +286,109 @@ __device__ __forceinline__ void s_softmax(Smem& sm, const Unit& u, const SplitPa
   const uint32_t xbuf0_remote = mapa_shared(xbuf0, peer);
   const uint32_t pfull_remote0 = mapa_shared(smem_u32(&sm.pfull[0]), peer);
   const uint32_t pfull_remote1 = mapa_shared(smem_u32(&sm.pfull[1]), peer);
-  const uint32_t ml_remote = mapa_shared(smem_u32(&sm.ml[0]), peer);
-  const uint32_t mlfull_remote = mapa_shared(smem_u32(&sm.mlfull), peer);
   const uint32_t xbytes = kPHead + (u.two_term ? 2u : 1u) * kPTerm;
 
+  // With a positive scale the row max is taken on raw scores and the scale is
+  // folded into the exp2 argument: p = 2^(s * a - m).  Otherwise the scores
+  // are scaled first and a_eff = 1.
   const float a = p.scale_log2;
+  const bool pos = a > 0.f;
+  const float a_eff = pos ? a : 1.f;
   float m_used = -CUDART_INF_F;   // log2-scaled running max actually used for P
-  float l = 0.f;                  // running sum of P
-
+  float l = 0.f;                  // this half's running sum of P
   bool copy_failed = false;       // set by the copy-issuing thread only
   bool finished = true;
+
   for (int j = 0; j < u.ntiles; ++j) {
     const int buf = j & 1;
     const bool got = warp_wait(sm, smem_u32(&sm.sfull[buf]), (j >> 1) & 1, p, 7);
-    if (named_bar_red_or(kSoftmaxBar, 128, !got || copy_failed)) {
+    uint32_t sr[32];
+    if (got) {
+      tc_fence_after();
+      MLA_TMEM_LD_32x32b_X32(tmem + lane_base + kQCols + 64 * buf + 32 * half, sr);
+      tmem_ld_wait();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&sm.sempty[buf]));
+      if (!pos) {
+#pragma unroll
+        for (int c = 0; c < 32; ++c) sr[c] = __float_as_uint(__uint_as_float(sr[c]) * a);
+      }
+      // Keys wholly inside the prefix are visible; otherwise bit c of `vis`
+      // says whether key key0+c is visible to this row.
+      const int key0 = u.k0 + j * kKeys + 32 * half;
+      if (!row_valid) {
+#pragma unroll
+        for (int c = 0; c < 32; ++c) sr[c] = __float_as_uint(-CUDART_INF_F);
+      } else if (key0 + 32 > u.prefix) {
+        const int np = u.prefix - key0;             // prefix keys in this half tile (may be <= 0)
+        uint32_t vis = np >= 32 ? ~0u : (np > 0 ? (1u << np) - 1u : 0u);
+        const uint64_t drafts = np > 0 ? mask64 << np : (-np < 64 ? mask64 >> (-np) : 0ull);
+        vis |= static_cast<uint32_t>(drafts);
+        const int nk = u.S - key0;                  // keys of the stream in this half tile
+        if (nk < 32) vis &= nk > 0 ? (1u << nk) - 1u : 0u;
+#pragma unroll
+        for (int c = 0; c < 32; ++c)
+          if (!((vis >> c) & 1u)) sr[c] = __float_as_uint(-CUDART_INF_F);
+      }
+      float mx[4];
+#pragma unroll
+      for (int k = 0; k < 4; ++k) mx[k] = __uint_as_float(sr[k]);
+#pragma unroll
+      for (int c = 4; c < 32; ++c) mx[c & 3] = fmaxf(mx[c & 3], __uint_as_float(sr[c]));
+      sm.xmax[half][r] = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * a_eff;
+    }
+    if (named_bar_red_or(kSoftmaxBar, kRowThreads, !got || copy_failed)) {
       finished = false;
       break;
     }
-    tc_fence_after();
-    uint32_t sr[64];
-    MLA_TMEM_LD_32x32b_X32(tmem + lane_base + kQCols + 64 * buf, sr);
-    MLA_TMEM_LD_32x32b_X32(tmem + lane_base + kQCols + 64 * buf + 32, (sr + 32));
-    tmem_ld_wait();
-    tc_fence_before();
-    __syncwarp();
-    if (lane == 0) mbar_arrive(smem_u32(&sm.sempty[buf]));
-
-    // Scaled scores y = s * scale * log2(e); masked keys get -inf.  Keys of a
-    // tile that lies wholly inside the prefix are all visible; otherwise bit c
-    // of `vis` says whether key key0+c is visible to this row.
-    const int key0 = u.k0 + j * kKeys;
+    const float mt = fmaxf(sm.xmax[0][r], sm.xmax[1][r]);
+    // Lazy rescale: P may exceed 1 by up to 2^kLazyRescale; O and l only get
+    // rescaled (here and in the O CTA) when the max grows beyond that.
     float alpha = 1.f;
     bool flag = false;
-    uint32_t hi[32], lo[32];
-    if (row_valid) {
-      if (key0 + kKeys <= u.prefix) {
-#pragma unroll
-        for (int c = 0; c < 64; ++c) sr[c] = __float_as_uint(__uint_as_float(sr[c]) * a);
-      } else {
-        const int np = u.prefix - key0;             // prefix keys in this tile (may be <= 0)
-        uint64_t vis = np >= 64 ? ~0ull : (np > 0 ? (1ull << np) - 1ull : 0ull);
-        uint64_t drafts = mask64;                   // bit j: draft j visible
-        if (np > 0) drafts = np >= 64 ? 0ull : drafts << np;
-        else drafts = drafts >> (-np);              // -np < q <= 64
-        vis |= drafts;
-        const int nk = u.S - key0;                  // keys of the stream in this tile
-        if (nk < 64) vis &= nk > 0 ? (1ull << nk) - 1ull : 0ull;
-#pragma unroll
-        for (int c = 0; c < 64; ++c)
-          sr[c] = ((vis >> c) & 1ull) ? __float_as_uint(__uint_as_float(sr[c]) * a)
-                                      : __float_as_uint(-CUDART_INF_F);
-      }
-      float mx[8];
-#pragma unroll
-      for (int k = 0; k < 8; ++k) mx[k] = __uint_as_float(sr[k]);
-#pragma unroll
-      for (int c = 8; c < 64; ++c) mx[c & 7] = fmaxf(mx[c & 7], __uint_as_float(sr[c]));
-      const float mt = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
-                             fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
-      // Lazy rescale: P may exceed 1 by up to 2^kLazyRescale; O and l only get
-      // rescaled (here and in the O CTA) when the max grows beyond that.
-      if (mt > m_used + kLazyRescale) {
-        alpha = ex2(m_used - mt);          // 0 when nothing was visible before
-        flag = (m_used != -CUDART_INF_F);  // an all-zero O row needs no rescale
-        m_used = mt;
-        l *= alpha;
-      }
-      const float msub = (m_used == -CUDART_INF_F) ? 0.f : m_used;
-      float ls[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-      for (int c = 0; c < 32; ++c) {
-        const float p0 = ex2(__uint_as_float(sr[2 * c]) - msub);
-        const float p1 = ex2(__uint_as_float(sr[2 * c + 1]) - msub);
-        ls[c & 3] += p0 + p1;
-        hi[c] = pack_bf16x2(p0, p1);
-        if (u.two_term) lo[c] = pack_bf16x2(p0 - bf16lo_to_f32(hi[c]), p1 - bf16hi_to_f32(hi[c]));
-      }
-      l += (ls[0] + ls[1]) + (ls[2] + ls[3]);
-    } else {
-      // Rows past the stream's q*H rows (the tail of the last row tile): P = 0.
-#pragma unroll
-      for (int c = 0; c < 32; ++c) hi[c] = lo[c] = 0u;
+    if (mt > m_used + kLazyRescale) {
+      alpha = ex2(m_used - mt);          // 0 when nothing was visible before
+      flag = (m_used != -CUDART_INF_F);  // an all-zero O row needs no rescale
+      m_used = mt;
+      l *= alpha;
     }
+    const float msub = (m_used == -CUDART_INF_F) ? 0.f : m_used;
 
-    // Stage [alpha | flags | P hi | P lo] locally, then one bulk copy into the
-    // O CTA.  The copy that last read this buffer (tile j-2) was waited for by
-    // its issuer before the barrier at the top of this iteration.
+    // P for 8 keys at a time, staged straight into buffer `buf` [alpha | flags
+    // | P hi | P lo]; one bulk copy then moves it into the O CTA.  The copy
+    // that last read this buffer (tile j-2) was waited for by its issuer
+    // before the barrier above.
     uint8_t* xb = sm.ring + kPOffset + buf * kPBuf;
-    reinterpret_cast<float*>(xb)[r] = alpha;
-    const uint32_t any = __any_sync(0xFFFFFFFFu, flag) ? 1u : 0u;
-    if (lane == 0) reinterpret_cast<uint32_t*>(xb + 512)[wq] = any;
     uint8_t* ph = xb + kPHead + r * 128;
+    float ls[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-    for (int q4 = 0; q4 < 8; ++q4)
-      *reinterpret_cast<uint4*>(ph + ((q4 ^ (r & 7)) << 4)) =
-          make_uint4(hi[4 * q4], hi[4 * q4 + 1], hi[4 * q4 + 2], hi[4 * q4 + 3]);
-    if (u.two_term) {
+    for (int q4 = 0; q4 < 4; ++q4) {
+      const int unit = 4 * half + q4;               // 16-byte unit = keys 8*unit .. 8*unit+7
+      uint32_t h[4], lw[4];
 #pragma unroll
-      for (int q4 = 0; q4 < 8; ++q4)
-        *reinterpret_cast<uint4*>(ph + kPTerm + ((q4 ^ (r & 7)) << 4)) =
-            make_uint4(lo[4 * q4], lo[4 * q4 + 1], lo[4 * q4 + 2], lo[4 * q4 + 3]);
+      for (int e = 0; e < 4; ++e) {
+        const int c = 4 * q4 + e;
+        const float p0 = ex2(fmaf(__uint_as_float(sr[2 * c]), a_eff, -msub));
+        const float p1 = ex2(fmaf(__uint_as_float(sr[2 * c + 1]), a_eff, -msub));
+        ls[e] += p0 + p1;
+        h[e] = pack_bf16x2(p0, p1);
+        lw[e] = u.two_term ? pack_bf16x2(p0 - bf16lo_to_f32(h[e]), p1 - bf16hi_to_f32(h[e])) : 0u;
+      }
+      *reinterpret_cast<uint4*>(ph + ((unit ^ (r & 7)) << 4)) = make_uint4(h[0], h[1], h[2], h[3]);
+      if (u.two_term)
+        *reinterpret_cast<uint4*>(ph + kPTerm + ((unit ^ (r & 7)) << 4)) =
+            make_uint4(lw[0], lw[1], lw[2], lw[3]);
+    }
+    l += (ls[0] + ls[1]) + (ls[2] + ls[3]);
+    if (half == 0) {
+      reinterpret_cast<float*>(xb)[r] = alpha;
+      const uint32_t any = __any_sync(0xFFFFFFFFu, flag) ? 1u : 0u;
+      if (lane == 0) reinterpret_cast<uint32_t*>(xb + 512)[wq] = any;
     }
     fence_proxy_async_smem();
-    named_bar_sync(kSoftmaxBar, 128);
-    if (r == 0) {
+    named_bar_sync(kSoftmaxBar, kRowThreads);
+    if (half == 0 && r == 0) {
       // The O CTA's buffer `buf` is free once its PV product of tile j-2 is done.
       if (wait_or_abort<true>(sm, smem_u32(&sm.pempty[buf]), ((j >> 1) & 1) ^ 1, p, 8)) {
         bulk_copy_to_peer(xbuf0_remote + buf * kPBuf, xbuf0 + buf * kPBuf, xbytes,
@@ -395,9 +400,13 @@ __device__ __forceinline__ void s_softmax(Smem& sm, const Unit& u, const SplitPa
       }
     }
   }
-  if (r == 0) bulk_wait_read<0>();
-  if (finished && !named_bar_red_or(kSoftmaxBar, 128, copy_failed))
-    st_async_v2(ml_remote + r * 8, __float_as_uint(m_used), __float_as_uint(l), mlfull_remote);
+  if (half == 0 && r == 0) bulk_wait_read<0>();
+  if (!finished) return;
+  if (half == 1) sm.xl[r] = l;
+  if (named_bar_red_or(kSoftmaxBar, kRowThreads, copy_failed)) return;
+  if (half == 0)
+    st_async_v2(mapa_shared(smem_u32(&sm.ml[r]), peer), __float_as_uint(m_used),
+                __float_as_uint(l + sm.xl[r]), mapa_shared(smem_u32(&sm.mlfull), peer));
 }
 
 // ============================================================ O CTA roles
@@ -484,11 +493,14 @@ __device__ __forceinline__ void o_mma(Smem& sm, const Unit& u, const SplitParams
   __syncwarp();
 }
 
+// Eight helper warps: warp 4+w and warp 8+w own tensor-memory lanes
+// 32w..32w+31 (one output row per lane) and split the 512 accumulator columns.
 __device__ __forceinline__ void o_helpers(Smem& sm, const Unit& u, const SplitParams& p,
-                                          uint32_t tmem, int wq, int lane) {
+                                          uint32_t tmem, int wq, int half, int lane) {
   const int r = wq * 32 + lane;
   const uint32_t lane_base = static_cast<uint32_t>(wq * 32) << 16;
-  const int tid = wq * 32 + lane;
+  const uint32_t col0 = 256u * half;
+  const int tid = half * 128 + wq * 32 + lane;
   int ncmd = 0;
   while (true) {
     if (!warp_wait(sm, smem_u32(&sm.corrgo), ncmd & 1, p, 14)) return;
@@ -502,7 +514,7 @@ __device__ __forceinline__ void o_helpers(Smem& sm, const Unit& u, const SplitPa
       const int z0 = u.k1 - (u.k0 + j * kKeys);
       const int nrow = kKeys - z0;
       uint8_t* tile = sm.ring + (j & 1) * kVTile;
-      for (int it = tid; it < nrow * kVChunks * 8; it += 128) {
+      for (int it = tid; it < nrow * kVChunks * 8; it += kRowThreads) {
         const int q4 = it & 7;
         const int rr = z0 + ((it >> 3) % nrow);
         const int c = (it >> 3) / nrow;
@@ -514,13 +526,13 @@ __device__ __forceinline__ void o_helpers(Smem& sm, const Unit& u, const SplitPa
       const float alpha = reinterpret_cast<const float*>(sm.ring + kPOffset + buf * kPBuf)[r];
       tc_fence_after();
       if (__any_sync(0xFFFFFFFFu, alpha != 1.f)) {
-        for (int cc = 0; cc < 16; ++cc) {
+        for (int cc = 0; cc < 8; ++cc) {
           uint32_t v[32];
-          MLA_TMEM_LD_32x32b_X32(tmem + lane_base + 32 * cc, v);
+          MLA_TMEM_LD_32x32b_X32(tmem + lane_base + col0 + 32 * cc, v);
           tmem_ld_wait();
 #pragma unroll
           for (int e = 0; e < 32; ++e) v[e] = __float_as_uint(__uint_as_float(v[e]) * alpha);
-          MLA_TMEM_ST_32x32b_X32(tmem + lane_base + 32 * cc, v);
+          MLA_TMEM_ST_32x32b_X32(tmem + lane_base + col0 + 32 * cc, v);
         }
         tmem_st_wait();
       }
@@ -546,14 +558,14 @@ __device__ __forceinline__ void o_helpers(Smem& sm, const Unit& u, const SplitPa
   } else {
     const size_t prow = static_cast<size_t>(u.sp) * p.B * u.rows_total + grow;
     dst = p.part_o + prow * kDl;
-    if (valid) p.part_ml[prow] = ml;
+    if (valid && half == 0) p.part_ml[prow] = ml;
   }
-  for (int cc = 0; cc < 16; ++cc) {
+  for (int cc = 0; cc < 8; ++cc) {
     uint32_t v[32];
-    MLA_TMEM_LD_32x32b_X32(tmem + lane_base + 32 * cc, v);
+    MLA_TMEM_LD_32x32b_X32(tmem + lane_base + col0 + 32 * cc, v);
     tmem_ld_wait();
     if (valid) {
-      float4* d4 = reinterpret_cast<float4*>(dst + 32 * cc);
+      float4* d4 = reinterpret_cast<float4*>(dst + col0 + 32 * cc);
 #pragma unroll
       for (int e = 0; e < 8; ++e)
         d4[e] = make_float4(__uint_as_float(v[4 * e]) * scale_out,
@@ -562,7 +574,7 @@ __device__ __forceinline__ void o_helpers(Smem& sm, const Unit& u, const SplitPa
                             __uint_as_float(v[4 * e + 3]) * scale_out);
     }
   }
-  if (direct && valid)
+  if (direct && valid && half == 0)
     p.lse[grow] = ml.y > 0.f ? (ml.x + log2f(ml.y)) * 0.6931471805599453f : -CUDART_INF_F;
   tc_fence_before();
 }
@@ -591,10 +603,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       mbar_init(smem_u32(&sm.kempty[i]), 1);
     }
     mbar_init(smem_u32(&sm.qfull), 1);
-    mbar_init(smem_u32(&sm.qready), 4);
+    mbar_init(smem_u32(&sm.qready), 8);
     for (int i = 0; i < 2; ++i) {
       mbar_init(smem_u32(&sm.sfull[i]), 1);
-      mbar_init(smem_u32(&sm.sempty[i]), 4);
+      mbar_init(smem_u32(&sm.sempty[i]), 8);
       mbar_init(smem_u32(&sm.pempty[i]), 1);
       mbar_init(smem_u32(&sm.pfull[i]), 1);
       mbar_init(smem_u32(&sm.vfull[i]), 1);
@@ -602,9 +614,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     }
     mbar_init(smem_u32(&sm.odone), 1);
     mbar_init(smem_u32(&sm.corrgo), 1);
-    mbar_init(smem_u32(&sm.corrdone), 4);
+    mbar_init(smem_u32(&sm.corrdone), 8);
     mbar_init(smem_u32(&sm.mlfull), 1);
     mbar_init(smem_u32(&sm.drain), 1);
+
     sm.abort_flag = 0;
     sm.cmd = 0;
     if (role == 1 && !u.empty) {
@@ -641,7 +654,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         mbar_wait(smem_u32(&sm.drain), 0, kWaitNs);
         __syncwarp();
       } else if (warp >= 4) {
-        s_softmax(sm, u, p, tmem, warp - 4, lane);
+        s_softmax(sm, u, p, tmem, warp & 3, (warp - 4) >> 2, lane);  // half = warp / 4 - 1
       }
     } else {
       if (warp == 0 && lane == 0) {
@@ -655,7 +668,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         mbar_wait(smem_u32(&sm.drain), 0, kWaitNs);
         __syncwarp();
       } else if (warp >= 4) {
-        o_helpers(sm, u, p, tmem, warp - 4, lane);
+        o_helpers(sm, u, p, tmem, warp & 3, (warp - 4) >> 2, lane);
       }
     }
   }
