@@ -122,6 +122,36 @@ const char* mla_verify_attn_strerror(int status);
 int mla_verify_attn_plan(int B, int q_len, int H, int Smax, int max_clusters, int* n_row_tiles,
                          int* nsplit, int* chunk_tiles);
 
+/*
+ * mla_verify_attn without a caller-provided workspace.  This entry point has no
+ * counterpart on the pages; it exists for callers that cannot allocate device
+ * memory for scratch: code whose device memory is entirely pre-planned by its
+ * own arena allocator (no way to hand out an extra buffer), latency-critical
+ * loops where cudaMalloc/cudaFree would synchronise the device, and plain C
+ * callers that link only this library and have no allocator of their own.
+ *
+ * Arguments and results are those of mla_verify_attn minus workspace and
+ * workspace_bytes.  The key-split partials live instead in one fixed scratch
+ * array of MLA_VERIFY_NOALLOC_SCRATCH_BYTES (32 MiB) compiled into this library
+ * (a file-scope __device__ array: every GPU that loads the library holds it
+ * until the process exits).  Calls whose partials need more than that return
+ * MLA_ERR_WORKSPACE and enqueue nothing; use mla_verify_attn with a workspace
+ * for them.  Nothing here calls cudaMalloc, cudaFree or any allocating routine.
+ *
+ * The first call on a device looks up the scratch array's device address
+ * (cudaGetSymbolAddress) and caches it; make that first call before any stream
+ * capture.  All calls on a device share that device's array, and it keeps the
+ * last call's contents; nothing in it needs to start at zero (each call writes
+ * every partial it later reads).  Calls on the same device that overlap on the
+ * GPU (e.g. issued to two streams without ordering between them) race on the
+ * array and may corrupt each other's results: order them, e.g. on one stream.
+ */
+#define MLA_VERIFY_NOALLOC_SCRATCH_BYTES ((size_t)32 << 20)
+int mla_verify_attn_noalloc(const void* q_nope_abs, const void* q_rope, const void* kv,
+                            const int32_t* seq_lens, const uint32_t* tree_mask, int B, int q_len,
+                            int H, int Smax, float scale, float* out, float* lse,
+                            cudaStream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

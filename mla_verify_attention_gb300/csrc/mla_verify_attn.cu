@@ -301,3 +301,48 @@ int mla_verify_attn_last_device_error(cudaStream_t stream) {
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// Scratch-free variant (declared in mla_verify_attn.h): for callers that cannot
+// allocate device memory, the key-split partials go to a fixed array compiled
+// into this library instead of a caller-provided workspace.
+namespace {
+
+// One copy per device that loads the library, held until the process exits.
+static __device__ __align__(256) unsigned char g_noalloc_scratch[MLA_VERIFY_NOALLOC_SCRATCH_BYTES];
+
+std::mutex g_noalloc_mutex;
+void* g_noalloc_addr[kMaxDevices];   // device address of g_noalloc_scratch, per device
+
+}  // namespace
+
+extern "C" int mla_verify_attn_noalloc(const void* q_nope_abs, const void* q_rope, const void* kv,
+                                       const int32_t* seq_lens, const uint32_t* tree_mask, int B,
+                                       int q_len, int H, int Smax, float scale, float* out,
+                                       float* lse, cudaStream_t stream) {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+    cudaGetLastError();
+    return MLA_ERR_UNSUPPORTED_DEVICE;
+  }
+  void* scratch = nullptr;
+  {
+    // First call on this device (which must be current): look up the array's
+    // device address once; host code cannot use the symbol itself.
+    std::lock_guard<std::mutex> lock(g_noalloc_mutex);
+    if (g_noalloc_addr[dev] == nullptr) {
+      void* addr = nullptr;
+      if (cudaGetSymbolAddress(&addr, g_noalloc_scratch) != cudaSuccess || addr == nullptr) {
+        cudaGetLastError();
+        return MLA_ERR_UNSUPPORTED_DEVICE;
+      }
+      g_noalloc_addr[dev] = addr;
+    }
+    scratch = g_noalloc_addr[dev];
+  }
+  // Invalid shapes report 0 here and are rejected by mla_verify_attn below.
+  if (mla_verify_attn_workspace_size(B, q_len, H, Smax) > MLA_VERIFY_NOALLOC_SCRATCH_BYTES)
+    return MLA_ERR_WORKSPACE;
+  return mla_verify_attn(q_nope_abs, q_rope, kv, seq_lens, tree_mask, B, q_len, H, Smax, scale,
+                         out, lse, scratch, MLA_VERIFY_NOALLOC_SCRATCH_BYTES, stream);
+}
