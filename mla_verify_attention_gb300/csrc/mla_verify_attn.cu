@@ -137,9 +137,10 @@ size_t workspace_bytes_for(int B, int q, int H, int nsplit) {
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
 
 int encode(DeviceInfo* d, CUtensorMap* map, const void* base, int rank, const cuuint64_t* dims,
-           const cuuint64_t* strides, const cuuint32_t* box) {
+           const cuuint64_t* strides, const cuuint32_t* box,
+           CUtensorMapDataType dtype = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16) {
   const cuuint32_t elem[4] = {1, 1, 1, 1};
-  const CUresult r = d->encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, const_cast<void*>(base),
+  const CUresult r = d->encode(map, dtype, rank, const_cast<void*>(base),
                                dims, strides, box, elem, CU_TENSOR_MAP_INTERLEAVE_NONE,
                                CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
@@ -237,13 +238,26 @@ int mla_verify_attn(const void* q_nope_abs, const void* q_rope, const void* kv,
     if (encode(d, &map_kvs, kv, 4, dims, strides, box_s) != MLA_OK) return MLA_ERR_LAUNCH;
     if (encode(d, &map_kvo, kv, 4, dims, strides, box_o) != MLA_OK) return MLA_ERR_LAUNCH;
   }
+  // Results: fp32 [slice][stream][q*H rows][512] (the slice partials, or `out`
+  // itself when the key range is not split), stored in [128 rows][32] boxes.
+  float* const part_o = static_cast<float*>(workspace);
+  CUtensorMap map_out;
+  {
+    const long long rps = static_cast<long long>(q_len) * H;   // rows per stream
+    const cuuint64_t dims[4] = {512, static_cast<cuuint64_t>(rps), static_cast<cuuint64_t>(B),
+                                static_cast<cuuint64_t>(ns)};
+    const cuuint64_t strides[3] = {512 * 4, static_cast<cuuint64_t>(rps) * 512 * 4,
+                                   static_cast<cuuint64_t>(rows) * 512 * 4};
+    const cuuint32_t box[4] = {32, mla::kRows, 1, 1};
+    if (encode(d, &map_out, ns > 1 ? static_cast<void*>(part_o) : static_cast<void*>(out), 4, dims,
+               strides, box, CU_TENSOR_MAP_DATA_TYPE_FLOAT32) != MLA_OK)
+      return MLA_ERR_LAUNCH;
+  }
 
   mla::SplitParams p;
   p.seq_lens = seq_lens;
   p.mask = tree_mask;
-  p.out = out;
   p.lse = lse;
-  p.part_o = static_cast<float*>(workspace);
   p.part_ml = ns > 1 ? reinterpret_cast<float2*>(static_cast<char*>(workspace) +
                                                  static_cast<size_t>(ns) * rows * 512 * 4)
                      : nullptr;
@@ -261,11 +275,11 @@ int mla_verify_attn(const void* q_nope_abs, const void* q_rope, const void* kv,
   const long long units = static_cast<long long>(B) * nrt * ns;
   if (2 * units >= (1LL << 31)) return MLA_ERR_SHAPE;
   mla::verify_split_kernel<<<static_cast<unsigned>(2 * units), mla::kThreads, kSmemBytes, stream>>>(
-      map_qn, map_qr, map_kvs, map_kvo, p);
+      map_qn, map_qr, map_kvs, map_kvo, map_out, p);
   if (cudaGetLastError() != cudaSuccess) return MLA_ERR_LAUNCH;
   if (ns > 1) {
     mla::CombineParams c;
-    c.part_o = p.part_o;
+    c.part_o = part_o;
     c.part_ml = p.part_ml;
     c.seq_lens = seq_lens;
     c.out = out;

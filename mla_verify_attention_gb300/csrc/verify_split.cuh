@@ -65,6 +65,10 @@ constexpr int kPOffset = kKSlots * kKTile;       // after the K ring / V tiles (
 constexpr int kThreads = 384;                    // 12 warps: 4 control + 8 row warps
 constexpr int kRingBytes = kPOffset + 2 * kPBuf;
 constexpr uint32_t kSoftmaxBar = 1;              // named barrier of the 8 softmax warps
+constexpr uint32_t kEpilogueBar = 2;             // O CTA: 2 and 3, one per half of the helpers
+constexpr int kOutBlock = kRows * 32 * 4;        // 16 KB: [128 rows][32 fp32 columns]
+constexpr int kOutBufs = 6;                      // staging blocks per helper half
+static_assert(2 * kOutBufs * kOutBlock <= kRingBytes, "epilogue staging must fit the ring");
 constexpr int kRowThreads = 256;                 // two threads per row (one per 32-key half)
 constexpr uint32_t kQCols = 288;                 // Q in tensor memory: 576 bf16 = 288 cols
 constexpr float kLazyRescale = 8.0f;             // log2 units: keep the max unless it grows by 2^8
@@ -81,10 +85,8 @@ enum : uint32_t { kStatusSeqLen = 1u, kStatusTimeout = 2u };
 struct SplitParams {
   const int32_t* seq_lens;
   const uint32_t* mask;
-  float* out;
   float* lse;
-  float* part_o;      // [nsplit][B*rows][512]
-  float2* part_ml;    // [nsplit][B*rows]
+  float2* part_ml;    // [nsplit][B*rows]; the outputs themselves go through the map_out tensor map
   unsigned int* status;
   int B, q, H, Smax;
   int n_rt, nsplit, chunk_tiles;
@@ -496,14 +498,19 @@ __device__ __forceinline__ void o_mma(Smem& sm, const Unit& u, const SplitParams
 // Eight helper warps: warp 4+w and warp 8+w own tensor-memory lanes
 // 32w..32w+31 (one output row per lane) and split the 512 accumulator columns.
 __device__ __forceinline__ void o_helpers(Smem& sm, const Unit& u, const SplitParams& p,
-                                          uint32_t tmem, int wq, int half, int lane) {
+                                          const CUtensorMap* map_out, uint32_t tmem, int wq,
+                                          int half, int lane) {
   const int r = wq * 32 + lane;
   const uint32_t lane_base = static_cast<uint32_t>(wq * 32) << 16;
   const uint32_t col0 = 256u * half;
   const int tid = half * 128 + wq * 32 + lane;
   int ncmd = 0;
+  bool failed = false;   // kept instead of returning: the epilogue's barriers need every warp
   while (true) {
-    if (!warp_wait(sm, smem_u32(&sm.corrgo), ncmd & 1, p, 14)) return;
+    if (!warp_wait(sm, smem_u32(&sm.corrgo), ncmd & 1, p, 14)) {
+      failed = true;
+      break;
+    }
     ++ncmd;
     const uint32_t cmd = *reinterpret_cast<volatile uint32_t*>(&sm.cmd);
     if (cmd == kCmdDone) break;
@@ -542,40 +549,56 @@ __device__ __forceinline__ void o_helpers(Smem& sm, const Unit& u, const SplitPa
     if (lane == 0) mbar_arrive(smem_u32(&sm.corrdone));
   }
 
-  // ---- epilogue
-  if (!warp_wait(sm, smem_u32(&sm.odone), 0, p, 15)) return;
-  if (!warp_wait<true>(sm, smem_u32(&sm.mlfull), 0, p, 16)) return;
+  // ---- epilogue.  Each half of the helper warps owns 256 of the 512 output
+  // columns: per 32-column block its 128 threads move their rows from tensor
+  // memory into a 128-byte-swizzled [128 rows][32] staging block in the (now
+  // idle) ring, and one thread writes the block with a TMA tensor store; rows
+  // past this stream's q*H rows lie outside the tensor map and are not written.
+  // The staging below uses named barriers: all 128 threads of a half decide
+  // together whether the results are complete.
+  const uint32_t bar = kEpilogueBar + static_cast<uint32_t>(half);
+  const bool ready = !failed && warp_wait(sm, smem_u32(&sm.odone), 0, p, 15) &&
+                     warp_wait<true>(sm, smem_u32(&sm.mlfull), 0, p, 16);
+  if (named_bar_red_or(bar, kRows, !ready)) return;
   tc_fence_after();
   const float2 ml = sm.ml[r];
   const bool valid = r < u.valid_rows;
   const size_t grow = static_cast<size_t>(u.b) * u.rows_total + u.row0 + r;  // global row
   const bool direct = p.nsplit == 1;
-  float* dst;
-  float scale_out = 1.f;
-  if (direct) {
-    dst = p.out + grow * kDl;
-    scale_out = ml.y > 0.f ? 1.f / ml.y : 0.f;
-  } else {
-    const size_t prow = static_cast<size_t>(u.sp) * p.B * u.rows_total + grow;
-    dst = p.part_o + prow * kDl;
-    if (valid && half == 0) p.part_ml[prow] = ml;
+  const float scale_out = direct ? (ml.y > 0.f ? 1.f / ml.y : 0.f) : 1.f;
+  if (valid && half == 0) {
+    if (direct)
+      p.lse[grow] = ml.y > 0.f ? (ml.x + log2f(ml.y)) * 0.6931471805599453f : -CUDART_INF_F;
+    else
+      p.part_ml[static_cast<size_t>(u.sp) * p.B * u.rows_total + grow] = ml;
   }
+  const bool issuer = wq == 0 && lane == 0;
   for (int cc = 0; cc < 8; ++cc) {
+    const int slot = cc < kOutBufs ? cc : cc - kOutBufs;
+    uint8_t* blk = sm.ring + (half * kOutBufs + slot) * kOutBlock;
+    if (cc == kOutBufs) {
+      // Blocks 0 and 1 reuse their staging buffers: their stores must have
+      // read them (at most kOutBufs - 2 of this thread's groups still reading).
+      if (issuer) bulk_wait_read<kOutBufs - 2>();
+      named_bar_sync(bar, kRows);
+    }
     uint32_t v[32];
     MLA_TMEM_LD_32x32b_X32(tmem + lane_base + col0 + 32 * cc, v);
     tmem_ld_wait();
-    if (valid) {
-      float4* d4 = reinterpret_cast<float4*>(dst + col0 + 32 * cc);
 #pragma unroll
-      for (int e = 0; e < 8; ++e)
-        d4[e] = make_float4(__uint_as_float(v[4 * e]) * scale_out,
-                            __uint_as_float(v[4 * e + 1]) * scale_out,
-                            __uint_as_float(v[4 * e + 2]) * scale_out,
-                            __uint_as_float(v[4 * e + 3]) * scale_out);
+    for (int e = 0; e < 8; ++e)
+      *reinterpret_cast<float4*>(blk + r * 128 + ((e ^ (r & 7)) << 4)) =
+          make_float4(__uint_as_float(v[4 * e]) * scale_out, __uint_as_float(v[4 * e + 1]) * scale_out,
+                      __uint_as_float(v[4 * e + 2]) * scale_out, __uint_as_float(v[4 * e + 3]) * scale_out);
+    fence_proxy_async_smem();
+    named_bar_sync(bar, kRows);
+    if (issuer) {
+      tma_store_4d(map_out, smem_u32(blk), static_cast<int>(col0) + 32 * cc, u.row0, u.b,
+                   direct ? 0 : u.sp);
+      bulk_commit_group();
     }
   }
-  if (direct && valid && half == 0)
-    p.lse[grow] = ml.y > 0.f ? (ml.x + log2f(ml.y)) * 0.6931471805599453f : -CUDART_INF_F;
+  if (issuer) bulk_wait_all();
   tc_fence_before();
 }
 
@@ -585,7 +608,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     verify_split_kernel(const __grid_constant__ CUtensorMap map_qn,
                         const __grid_constant__ CUtensorMap map_qr,
                         const __grid_constant__ CUtensorMap map_kvs,
-                        const __grid_constant__ CUtensorMap map_kvo, const SplitParams p) {
+                        const __grid_constant__ CUtensorMap map_kvo,
+                        const __grid_constant__ CUtensorMap map_out, const SplitParams p) {
   extern __shared__ uint8_t smem_raw[];
   Smem& sm = *reinterpret_cast<Smem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                       ~static_cast<uintptr_t>(1023));
@@ -659,6 +683,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     } else {
       if (warp == 0 && lane == 0) {
         tma_prefetch_desc(&map_kvo);
+        tma_prefetch_desc(&map_out);
         int n_issued = 0;
         o_producer(sm, u, p, &map_kvo, n_issued);
         drain_ring(sm.vfull, kVSlots, n_issued);
@@ -668,7 +693,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         mbar_wait(smem_u32(&sm.drain), 0, kWaitNs);
         __syncwarp();
       } else if (warp >= 4) {
-        o_helpers(sm, u, p, tmem, warp & 3, (warp - 4) >> 2, lane);
+        o_helpers(sm, u, p, &map_out, tmem, warp & 3, (warp - 4) >> 2, lane);
       }
     }
   }
