@@ -217,7 +217,7 @@ int mla_verify_attn(const void* q_nope_abs, const void* q_rope, const void* kv,
   // chunks of 64 dims; the chunk index is its own dimension (stride 128 B) so
   // that one TMA box brings [chunk][row][64 dims] into shared memory, i.e. a
   // whole 64-key tile per copy, in the 128-byte-swizzled layout the MMAs read.
-  CUtensorMap map_qn, map_qr, map_kvs, map_kvo;
+  CUtensorMap map_qn, map_qr, map_kvs0, map_kvs1, map_kvo;
   {
     const cuuint64_t dims[3] = {64, static_cast<cuuint64_t>(rows), 8};
     const cuuint64_t strides[2] = {512 * 2, 64 * 2};
@@ -233,9 +233,12 @@ int mla_verify_attn(const void* q_nope_abs, const void* q_rope, const void* kv,
   {
     const cuuint64_t dims[4] = {64, static_cast<cuuint64_t>(Smax), 9, static_cast<cuuint64_t>(B)};
     const cuuint64_t strides[3] = {576 * 2, 64 * 2, static_cast<cuuint64_t>(Smax) * 576 * 2};
-    const cuuint32_t box_s[4] = {64, mla::kKeys, 9, 1};
+    // S CTA: a key tile's chunks 0..4 and 5..8 as two boxes; O CTA: chunks 0..7.
+    const cuuint32_t box_s0[4] = {64, mla::kKeys, mla::kKSplit, 1};
+    const cuuint32_t box_s1[4] = {64, mla::kKeys, 9 - mla::kKSplit, 1};
     const cuuint32_t box_o[4] = {64, mla::kKeys, 8, 1};
-    if (encode(d, &map_kvs, kv, 4, dims, strides, box_s) != MLA_OK) return MLA_ERR_LAUNCH;
+    if (encode(d, &map_kvs0, kv, 4, dims, strides, box_s0) != MLA_OK) return MLA_ERR_LAUNCH;
+    if (encode(d, &map_kvs1, kv, 4, dims, strides, box_s1) != MLA_OK) return MLA_ERR_LAUNCH;
     if (encode(d, &map_kvo, kv, 4, dims, strides, box_o) != MLA_OK) return MLA_ERR_LAUNCH;
   }
   // Results: fp32 [slice][stream][q*H rows][512] (the slice partials, or `out`
@@ -275,7 +278,7 @@ int mla_verify_attn(const void* q_nope_abs, const void* q_rope, const void* kv,
   const long long units = static_cast<long long>(B) * nrt * ns;
   if (2 * units >= (1LL << 31)) return MLA_ERR_SHAPE;
   mla::verify_split_kernel<<<static_cast<unsigned>(2 * units), mla::kThreads, kSmemBytes, stream>>>(
-      map_qn, map_qr, map_kvs, map_kvo, map_out, p);
+      map_qn, map_qr, map_kvs0, map_kvs1, map_kvo, map_out, p);
   if (cudaGetLastError() != cudaSuccess) return MLA_ERR_LAUNCH;
   if (ns > 1) {
     mla::CombineParams c;

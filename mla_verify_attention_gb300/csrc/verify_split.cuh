@@ -53,7 +53,10 @@ constexpr int kKChunks = 9;                      // 576 / 64
 constexpr int kVChunks = 8;                      // 512 / 64
 constexpr int kKSlots = 2;                       // S CTA key-tile ring: 2 x 72 KB
 constexpr int kVSlots = 2;                       // O CTA value-tile ring: 2 x 64 KB
-constexpr int kKTile = kKChunks * kChunk;        // 72 KB: one TMA box per tile
+constexpr int kKTile = kKChunks * kChunk;        // 72 KB per key tile, loaded as two boxes:
+constexpr int kKSplit = 5;                       //   part 0 = chunks 0..4 (40 KB),
+constexpr int kKPart0 = kKSplit * kChunk;        //   part 1 = chunks 5..8 (32 KB), each with
+constexpr int kKPart1 = kKTile - kKPart0;        //   its own full / empty barriers
 constexpr int kVTile = kVChunks * kChunk;        // 64 KB: one TMA box per tile
 constexpr int kPTerm = kRows * kKeys * 2;        // 16 KB per P term
 // One P exchange buffer: [alpha: 128 f32 | flags: 4 u32 | pad][P hi][P lo].
@@ -99,7 +102,7 @@ struct __align__(1024) Smem {
   float2 ml[kRows];
   float xmax[2][kRows];      // S CTA: per-half partial row max of the current tile
   float xl[kRows];           // S CTA: second half's running sum, combined at the end
-  uint64_t kfull[kKSlots], kempty[kKSlots];
+  uint64_t kfull[2][kKSlots], kempty[2][kKSlots];   // [part][slot]
   uint64_t qfull, qready;
   uint64_t sfull[2], sempty[2];
   uint64_t pempty[2];
@@ -189,7 +192,8 @@ __device__ __forceinline__ void drain_ring(const uint64_t* full, int nslots, int
 
 __device__ __forceinline__ void s_producer(Smem& sm, const Unit& u, const SplitParams& p,
                                            const CUtensorMap* map_qn, const CUtensorMap* map_qr,
-                                           const CUtensorMap* map_kv, int& n_issued) {
+                                           const CUtensorMap* map_kv0, const CUtensorMap* map_kv1,
+                                           int* n_issued) {
   const uint32_t ring = smem_u32(sm.ring);
   const uint32_t qfull = smem_u32(&sm.qfull);
   // Q rows of this unit: 8 latent chunks + 1 rope chunk of [128 rows x 64 dims].
@@ -202,14 +206,21 @@ __device__ __forceinline__ void s_producer(Smem& sm, const Unit& u, const SplitP
   // warps have moved Q into tensor memory.
   if (!wait_or_abort(sm, smem_u32(&sm.qready), 0, p, 1)) return;
   fence_proxy_async();
-  // One box per 64-key tile: [9 chunks][64 keys][64 dims].
+  // Two boxes per 64-key tile: [5 chunks][64 keys][64 dims] and [4 chunks][64][64].
+  // A part's buffer is refilled as soon as the MMAs that read it are done, so
+  // the first chunks of tile j+2 load while the last ones of tile j are used.
   for (int j = 0; j < u.ntiles; ++j) {
     const int slot = j % kKSlots;
-    if (!wait_or_abort(sm, smem_u32(&sm.kempty[slot]), ((j / kKSlots) & 1) ^ 1, p, 2)) return;
-    const uint32_t full = smem_u32(&sm.kfull[slot]);
-    mbar_arrive_expect_tx(full, kKTile);
-    tma_load_4d(ring + slot * kKTile, map_kv, 0, u.k0 + j * kKeys, 0, u.b, full);
-    n_issued = j + 1;
+#pragma unroll
+    for (int part = 0; part < 2; ++part) {
+      if (!wait_or_abort(sm, smem_u32(&sm.kempty[part][slot]), ((j / kKSlots) & 1) ^ 1, p, 2))
+        return;
+      const uint32_t full = smem_u32(&sm.kfull[part][slot]);
+      mbar_arrive_expect_tx(full, part ? kKPart1 : kKPart0);
+      tma_load_4d(ring + slot * kKTile + part * kKPart0, part ? map_kv1 : map_kv0, 0,
+                  u.k0 + j * kKeys, part ? kKSplit : 0, u.b, full);
+      n_issued[part] = j + 1;
+    }
   }
 }
 
@@ -226,15 +237,22 @@ __device__ __forceinline__ void s_mma(Smem& sm, const Unit& u, const SplitParams
     tc_fence_after();
     const uint32_t d = tmem + kQCols + 64 * buf;
     const int slot = j % kKSlots;
-    if (!warp_wait(sm, smem_u32(&sm.kfull[slot]), (j / kKSlots) & 1, p, 5)) return;
-    tc_fence_after();
     // Descriptor of chunk c = descriptor of chunk 0 + c * 8 KB (in 16-byte units).
     const uint64_t bdesc0 = sdesc_sw128(ring + slot * kKTile, 16, 1024);
+    if (!warp_wait(sm, smem_u32(&sm.kfull[0][slot]), (j / kKSlots) & 1, p, 5)) return;
+    tc_fence_after();
 #pragma unroll
-    for (int c = 0; c < kKChunks; ++c)
+    for (int c = 0; c < kKSplit; ++c)
       mma_ts_chunk_elect(d, tmem + c * 32, bdesc0 + static_cast<uint64_t>(c * (kChunk >> 4)),
                          kIdescQK, c != 0);
-    mma_commit_elect(smem_u32(&sm.kempty[slot]));
+    mma_commit_elect(smem_u32(&sm.kempty[0][slot]));
+    if (!warp_wait(sm, smem_u32(&sm.kfull[1][slot]), (j / kKSlots) & 1, p, 5)) return;
+    tc_fence_after();
+#pragma unroll
+    for (int c = kKSplit; c < kKChunks; ++c)
+      mma_ts_chunk_elect(d, tmem + c * 32, bdesc0 + static_cast<uint64_t>(c * (kChunk >> 4)),
+                         kIdescQK, 1u);
+    mma_commit_elect(smem_u32(&sm.kempty[1][slot]));
     mma_commit_elect(smem_u32(&sm.sfull[buf]));
   }
 }
@@ -243,6 +261,8 @@ __device__ __forceinline__ void s_mma(Smem& sm, const Unit& u, const SplitParams
 // 32w..32w+31 (one query row per lane); the first takes keys 0..31 of each
 // tile, the second keys 32..63.  The two halves agree on the row max through
 // shared memory once per tile; each keeps its own part of the running sum.
+// kTwoTerm: P goes out as two bf16 terms hi + lo (short streams).
+template <bool kTwoTerm>
 __device__ __forceinline__ void s_softmax(Smem& sm, const Unit& u, const SplitParams& p,
                                           uint32_t tmem, int wq, int half, int lane) {
   const int r = wq * 32 + lane;                     // row of the unit == tensor-memory lane
@@ -288,7 +308,7 @@ __device__ __forceinline__ void s_softmax(Smem& sm, const Unit& u, const SplitPa
   const uint32_t xbuf0_remote = mapa_shared(xbuf0, peer);
   const uint32_t pfull_remote0 = mapa_shared(smem_u32(&sm.pfull[0]), peer);
   const uint32_t pfull_remote1 = mapa_shared(smem_u32(&sm.pfull[1]), peer);
-  const uint32_t xbytes = kPHead + (u.two_term ? 2u : 1u) * kPTerm;
+  const uint32_t xbytes = kPHead + (kTwoTerm ? 2u : 1u) * kPTerm;
 
   // With a positive scale the row max is taken on raw scores and the scale is
   // folded into the exp2 argument: p = 2^(s * a - m).  Otherwise the scores
@@ -363,7 +383,10 @@ __device__ __forceinline__ void s_softmax(Smem& sm, const Unit& u, const SplitPa
     // before the barrier above.
     uint8_t* xb = sm.ring + kPOffset + buf * kPBuf;
     uint8_t* ph = xb + kPHead + r * 128;
-    float ls[4] = {0.f, 0.f, 0.f, 0.f};
+    // Exponent arguments and running sums in packed fp32 pairs.
+    const uint64_t a2 = f2pack(a_eff, a_eff);
+    const uint64_t m2 = f2pack(-msub, -msub);
+    uint64_t ls2[2] = {0ull, 0ull};                 // bit pattern 0 = (0.f, 0.f)
 #pragma unroll
     for (int q4 = 0; q4 < 4; ++q4) {
       const int unit = 4 * half + q4;               // 16-byte unit = keys 8*unit .. 8*unit+7
@@ -371,18 +394,26 @@ __device__ __forceinline__ void s_softmax(Smem& sm, const Unit& u, const SplitPa
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
         const int c = 4 * q4 + e;
-        const float p0 = ex2(fmaf(__uint_as_float(sr[2 * c]), a_eff, -msub));
-        const float p1 = ex2(fmaf(__uint_as_float(sr[2 * c + 1]), a_eff, -msub));
-        ls[e] += p0 + p1;
+        float x0, x1;
+        f2unpack(ffma2(f2pack(__uint_as_float(sr[2 * c]), __uint_as_float(sr[2 * c + 1])), a2, m2),
+                 x0, x1);
+        const float p0 = ex2(x0);
+        const float p1 = ex2(x1);
+        ls2[e & 1] = fadd2(ls2[e & 1], f2pack(p0, p1));
         h[e] = pack_bf16x2(p0, p1);
-        lw[e] = u.two_term ? pack_bf16x2(p0 - bf16lo_to_f32(h[e]), p1 - bf16hi_to_f32(h[e])) : 0u;
+        if (kTwoTerm) lw[e] = pack_bf16x2(p0 - bf16lo_to_f32(h[e]), p1 - bf16hi_to_f32(h[e]));
       }
       *reinterpret_cast<uint4*>(ph + ((unit ^ (r & 7)) << 4)) = make_uint4(h[0], h[1], h[2], h[3]);
-      if (u.two_term)
+      if (kTwoTerm)
         *reinterpret_cast<uint4*>(ph + kPTerm + ((unit ^ (r & 7)) << 4)) =
             make_uint4(lw[0], lw[1], lw[2], lw[3]);
     }
-    l += (ls[0] + ls[1]) + (ls[2] + ls[3]);
+    {
+      float s0, s1, s2, s3;
+      f2unpack(ls2[0], s0, s1);
+      f2unpack(ls2[1], s2, s3);
+      l += (s0 + s1) + (s2 + s3);
+    }
     if (half == 0) {
       reinterpret_cast<float*>(xb)[r] = alpha;
       const uint32_t any = __any_sync(0xFFFFFFFFu, flag) ? 1u : 0u;
@@ -607,7 +638,8 @@ __device__ __forceinline__ void o_helpers(Smem& sm, const Unit& u, const SplitPa
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     verify_split_kernel(const __grid_constant__ CUtensorMap map_qn,
                         const __grid_constant__ CUtensorMap map_qr,
-                        const __grid_constant__ CUtensorMap map_kvs,
+                        const __grid_constant__ CUtensorMap map_kvs0,
+                        const __grid_constant__ CUtensorMap map_kvs1,
                         const __grid_constant__ CUtensorMap map_kvo,
                         const __grid_constant__ CUtensorMap map_out, const SplitParams p) {
   extern __shared__ uint8_t smem_raw[];
@@ -623,8 +655,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     if ((u.S < p.q || u.S > p.Smax) && role == 0 && u.sp == 0 && u.rt == 0)
       atomicOr(p.status, kStatusSeqLen);
     for (int i = 0; i < kKSlots; ++i) {
-      mbar_init(smem_u32(&sm.kfull[i]), 1);
-      mbar_init(smem_u32(&sm.kempty[i]), 1);
+      for (int part = 0; part < 2; ++part) {
+        mbar_init(smem_u32(&sm.kfull[part][i]), 1);
+        mbar_init(smem_u32(&sm.kempty[part][i]), 1);
+      }
     }
     mbar_init(smem_u32(&sm.qfull), 1);
     mbar_init(smem_u32(&sm.qready), 8);
@@ -667,18 +701,23 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       if (warp == 0 && lane == 0) {
         tma_prefetch_desc(&map_qn);
         tma_prefetch_desc(&map_qr);
-        tma_prefetch_desc(&map_kvs);
-        int n_issued = 0;
-        s_producer(sm, u, p, &map_qn, &map_qr, &map_kvs, n_issued);
+        tma_prefetch_desc(&map_kvs0);
+        tma_prefetch_desc(&map_kvs1);
+        int n_issued[2] = {0, 0};
+        s_producer(sm, u, p, &map_qn, &map_qr, &map_kvs0, &map_kvs1, n_issued);
         mbar_wait(smem_u32(&sm.qfull), 0, kWaitNs / 2);
-        drain_ring(sm.kfull, kKSlots, n_issued);
+        drain_ring(sm.kfull[0], kKSlots, n_issued[0]);
+        drain_ring(sm.kfull[1], kKSlots, n_issued[1]);
       } else if (warp == 1) {
         s_mma(sm, u, p, tmem);
         mma_commit_elect(smem_u32(&sm.drain));
         mbar_wait(smem_u32(&sm.drain), 0, kWaitNs);
         __syncwarp();
       } else if (warp >= 4) {
-        s_softmax(sm, u, p, tmem, warp & 3, (warp - 4) >> 2, lane);  // half = warp / 4 - 1
+        if (u.two_term)
+          s_softmax<true>(sm, u, p, tmem, warp & 3, (warp - 4) >> 2, lane);  // half = warp / 4 - 1
+        else
+          s_softmax<false>(sm, u, p, tmem, warp & 3, (warp - 4) >> 2, lane);
       }
     } else {
       if (warp == 0 && lane == 0) {
