@@ -8,7 +8,7 @@
 // lse = (M + log2 L) ln 2.  Slices with l_s = 0 are skipped (their O_s is 0).
 //
 // Memory-bound: one 128-thread block per query row, 16-byte loads and stores,
-// fully coalesced over the 512-wide rows.
+// fully coalesced over the 512-wide rows; up to 16 slices' loads in flight.
 #pragma once
 #include <cstdint>
 #include <math_constants.h>
@@ -28,7 +28,17 @@ struct CombineParams {
   int q, Smax, nsplit, chunk_keys;
 };
 
-__global__ void __launch_bounds__(128) combine_kernel(const CombineParams p) {
+constexpr int kCombineBatch = 16;   // slices whose loads are in flight together
+
+// Launched as a programmatic dependent of the split kernel: the block may start
+// while that grid still runs and waits here until its results are visible.
+__device__ __forceinline__ void wait_for_split_grid() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+// Four blocks per SM (<= 128 registers): all rows of a 64-head, 9-draft call in one wave.
+__global__ void __launch_bounds__(128, 4) combine_kernel(const CombineParams p) {
+  wait_for_split_grid();
   const int row = blockIdx.x;
   const int tid = threadIdx.x;
   const int b = row / p.rows_per_stream;
@@ -36,43 +46,50 @@ __global__ void __launch_bounds__(128) combine_kernel(const CombineParams p) {
   if (S < p.q || S > p.Smax) return;   // reported by the split kernel
   const int ns = min(p.nsplit, (S + p.chunk_keys - 1) / p.chunk_keys);
   const float2* ml = p.part_ml + row;
-  float M = -CUDART_INF_F;
-#pragma unroll 8
-  for (int s = 0; s < ns; ++s) {
-    const float2 v = ml[static_cast<size_t>(s) * p.N];
-    M = v.y > 0.f ? fmaxf(M, v.x) : M;
+  const float4* src = reinterpret_cast<const float4*>(p.part_o + static_cast<size_t>(row) * 512) + tid;
+  const size_t step4 = static_cast<size_t>(p.N) * 128;   // float4s between slices
+  // Every slice s < ns wrote its partial (an all-zero accumulator where no key
+  // was visible).  A batch's (m, l) pairs and accumulators are all requested
+  // before any is used; batches are merged online (running max M).
+  float M = -CUDART_INF_F, L = 0.f;
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int s0 = 0; s0 < ns; s0 += kCombineBatch) {
+    float2 v[kCombineBatch];
+    float4 o[kCombineBatch];
+#pragma unroll
+    for (int e = 0; e < kCombineBatch; ++e) {
+      const int s = s0 + e;
+      if (s < ns) {
+        v[e] = ml[static_cast<size_t>(s) * p.N];
+        o[e] = src[s * step4];
+      } else {
+        v[e] = make_float2(-CUDART_INF_F, 0.f);
+        o[e] = make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+    }
+    float Mb = M;
+#pragma unroll
+    for (int e = 0; e < kCombineBatch; ++e) Mb = v[e].y > 0.f ? fmaxf(Mb, v[e].x) : Mb;
+    if (Mb == -CUDART_INF_F) continue;            // nothing visible so far
+    const float c = ex2(M - Mb);                  // 0 while M = -inf (L, acc are 0 then)
+    L *= c;
+    acc.x *= c; acc.y *= c; acc.z *= c; acc.w *= c;
+#pragma unroll
+    for (int e = 0; e < kCombineBatch; ++e) {
+      const float w = v[e].y > 0.f ? ex2(v[e].x - Mb) : 0.f;
+      L += w * v[e].y;
+      acc.x += w * o[e].x;
+      acc.y += w * o[e].y;
+      acc.z += w * o[e].z;
+      acc.w += w * o[e].w;
+    }
+    M = Mb;
   }
   float4* dst = reinterpret_cast<float4*>(p.out + static_cast<size_t>(row) * 512) + tid;
   if (M == -CUDART_INF_F) {
     *dst = make_float4(0.f, 0.f, 0.f, 0.f);
     if (tid == 0) p.lse[row] = -CUDART_INF_F;
     return;
-  }
-  // Every slice s < ns wrote its partial (an all-zero accumulator where no key
-  // was visible), so the loads are unconditional: eight independent 16-byte
-  // loads are in flight per thread.
-  float L = 0.f;
-  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-  const float4* src = reinterpret_cast<const float4*>(p.part_o + static_cast<size_t>(row) * 512) + tid;
-  const size_t step4 = static_cast<size_t>(p.N) * 128;   // float4s between slices
-  for (int s0 = 0; s0 < ns; s0 += 8) {
-    float4 o[8];
-    float w[8];
-#pragma unroll
-    for (int e = 0; e < 8; ++e) {
-      const int s = min(s0 + e, ns - 1);
-      o[e] = src[s * step4];
-      const float2 v = ml[static_cast<size_t>(s) * p.N];
-      w[e] = (s0 + e < ns && v.y > 0.f) ? ex2(v.x - M) : 0.f;
-      L += w[e] * (s0 + e < ns ? v.y : 0.f);
-    }
-#pragma unroll
-    for (int e = 0; e < 8; ++e) {
-      acc.x += w[e] * o[e].x;
-      acc.y += w[e] * o[e].y;
-      acc.z += w[e] * o[e].z;
-      acc.w += w[e] * o[e].w;
-    }
   }
   const float inv = 1.f / L;
   *dst = make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);

@@ -293,8 +293,22 @@ int mla_verify_attn(const void* q_nope_abs, const void* q_rope, const void* kv,
     c.Smax = Smax;
     c.nsplit = ns;
     c.chunk_keys = ct * mla::kKeys;
-    mla::combine_kernel<<<static_cast<unsigned>(rows), 128, 0, stream>>>(c);
-    if (cudaGetLastError() != cudaSuccess) return MLA_ERR_LAUNCH;
+    // Programmatic dependent launch: the merge blocks may be scheduled while
+    // the split kernel drains and wait (griddepcontrol.wait) for its results.
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(rows), 1, 1);
+    cfg.blockDim = dim3(128, 1, 1);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaLaunchKernelEx(&cfg, mla::combine_kernel, c) != cudaSuccess) {
+      cudaGetLastError();
+      return MLA_ERR_LAUNCH;
+    }
   }
   return MLA_OK;
 }

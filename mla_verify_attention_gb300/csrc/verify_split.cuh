@@ -604,18 +604,24 @@ __device__ __forceinline__ void o_helpers(Smem& sm, const Unit& u, const SplitPa
       p.part_ml[static_cast<size_t>(u.sp) * p.B * u.rows_total + grow] = ml;
   }
   const bool issuer = wq == 0 && lane == 0;
+  // Tensor-memory loads run one block ahead: block cc+1 is requested before
+  // block cc is staged (tcgen05.wait::ld then waits for it at the next step).
+  uint32_t va[32], vb[32];
+  MLA_TMEM_LD_32x32b_X32(tmem + lane_base + col0, va);
+  tmem_ld_wait();
+#pragma unroll
   for (int cc = 0; cc < 8; ++cc) {
     const int slot = cc < kOutBufs ? cc : cc - kOutBufs;
     uint8_t* blk = sm.ring + (half * kOutBufs + slot) * kOutBlock;
+    uint32_t* v = (cc & 1) ? vb : va;
+    uint32_t* vn = (cc & 1) ? va : vb;
+    if (cc + 1 < 8) MLA_TMEM_LD_32x32b_X32(tmem + lane_base + col0 + 32 * (cc + 1), vn);
     if (cc == kOutBufs) {
       // Blocks 0 and 1 reuse their staging buffers: their stores must have
       // read them (at most kOutBufs - 2 of this thread's groups still reading).
       if (issuer) bulk_wait_read<kOutBufs - 2>();
       named_bar_sync(bar, kRows);
     }
-    uint32_t v[32];
-    MLA_TMEM_LD_32x32b_X32(tmem + lane_base + col0 + 32 * cc, v);
-    tmem_ld_wait();
 #pragma unroll
     for (int e = 0; e < 8; ++e)
       *reinterpret_cast<float4*>(blk + r * 128 + ((e ^ (r & 7)) << 4)) =
@@ -628,6 +634,7 @@ __device__ __forceinline__ void o_helpers(Smem& sm, const Unit& u, const SplitPa
                    direct ? 0 : u.sp);
       bulk_commit_group();
     }
+    if (cc + 1 < 8) tmem_ld_wait();
   }
   if (issuer) bulk_wait_all();
   tc_fence_before();
@@ -650,6 +657,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   const int lane = tid & 31;
   const uint32_t role = cluster_ctarank();   // 0: scores + softmax, 1: PV accumulator
   const Unit u = decode_unit(p);
+  // The slice merge is launched as a programmatic dependent of this grid; it
+  // may be scheduled now and waits for this grid's completion itself.
+  if (tid == 0) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
   if (tid == 0) {
     if ((u.S < p.q || u.S > p.Smax) && role == 0 && u.sp == 0 && u.rt == 0)
