@@ -30,6 +30,12 @@
  *     recorded in a per-device status word read by mla_verify_attn_last_device_error.
  *   - bf16 tensors are passed as `const void*` holding IEEE bfloat16 values.
  *   - Results are deterministic for fixed inputs, Smax and device.
+ *   - Stream capture: no entry point reads device memory on the host or
+ *     synchronises inside mla_verify_attn.  Grid, split plan and tensor maps
+ *     depend only on (B, q_len, H, Smax), the pointers and the device, so after
+ *     the first call on a device (one-time setup: kernel attributes, occupancy
+ *     query) a call may be captured into a CUDA graph; each replay reads the
+ *     inputs' contents at replay time (seq_lens may change, within Smax).
  */
 #ifndef MLA_VERIFY_ATTN_H
 #define MLA_VERIFY_ATTN_H
@@ -146,6 +152,19 @@ int mla_verify_attn_plan(int B, int q_len, int H, int Smax, int max_clusters, in
  * GPU (e.g. issued to two streams without ordering between them) race on the
  * array and may corrupt each other's results: order them, e.g. on one stream.
  */
+/*
+ * Measurement aid; the pages have no counterpart.  While both events are
+ * non-NULL, every mla_verify_attn call records `before_split` on its stream
+ * just before the split kernel is launched and `after_split` just after it, so
+ * cudaEventElapsedTime(before_split, after_split) is the split kernel's own
+ * duration.  While they are set, the slice merge is launched without overlapping
+ * the split kernel's tail.  NULL, NULL switches recording off.  The events are
+ * the caller's (cudaEventCreate); the library only records them.  Set this only
+ * while no other thread is calling into the library.  Returns MLA_OK, or
+ * MLA_ERR_NULLPTR when exactly one event is NULL.
+ */
+int mla_verify_attn_set_timing_events(cudaEvent_t before_split, cudaEvent_t after_split);
+
 #define MLA_VERIFY_NOALLOC_SCRATCH_BYTES ((size_t)32 << 20)
 int mla_verify_attn_noalloc(const void* q_nope_abs, const void* q_rope, const void* kv,
                             const int32_t* seq_lens, const uint32_t* tree_mask, int B, int q_len,

@@ -51,6 +51,8 @@ def load_library(build_if_missing: bool = True) -> ctypes.CDLL:
         IP = ctypes.POINTER(ctypes.c_int)
         lib.mla_verify_attn_plan.argtypes = [I, I, I, I, I, IP, IP, IP]
         lib.mla_verify_attn_plan.restype = I
+        lib.mla_verify_attn_set_timing_events.argtypes = [P, P]
+        lib.mla_verify_attn_set_timing_events.restype = I
         _lib = lib
         return lib
 
@@ -127,6 +129,19 @@ def verify_attn(q_nope, q_rope, kv, seq_lens, tree_mask, scale, out=None, lse=No
     if st != MLA_OK:
         raise MLAError(st)
     return out, lse
+
+
+def set_timing_events(before=None, after=None) -> None:
+    """Have every later call record two torch.cuda.Events around its split kernel.
+
+    The events must already exist on the device (record each once first: torch
+    creates them lazily).  ``set_timing_events()`` switches recording off.
+    """
+    b = 0 if before is None else int(before.cuda_event)
+    a = 0 if after is None else int(after.cuda_event)
+    st = int(load_library().mla_verify_attn_set_timing_events(b or None, a or None))
+    if st != MLA_OK:
+        raise MLAError(st, "mla_verify_attn_set_timing_events")
 
 
 def last_device_error(stream=None) -> int:

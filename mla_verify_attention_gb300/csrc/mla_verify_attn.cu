@@ -37,6 +37,10 @@ struct DeviceInfo {
 std::mutex g_mutex;
 DeviceInfo g_devices[kMaxDevices];
 
+// Events recorded around the split kernel (mla_verify_attn_set_timing_events).
+cudaEvent_t g_timing_before = nullptr;
+cudaEvent_t g_timing_after = nullptr;
+
 int device_info(DeviceInfo** out) {
   int dev = -1;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
@@ -277,9 +281,18 @@ int mla_verify_attn(const void* q_nope_abs, const void* q_rope, const void* kv,
 
   const long long units = static_cast<long long>(B) * nrt * ns;
   if (2 * units >= (1LL << 31)) return MLA_ERR_SHAPE;
+  const bool timing = g_timing_before != nullptr;
+  if (timing && cudaEventRecord(g_timing_before, stream) != cudaSuccess) {
+    cudaGetLastError();
+    return MLA_ERR_LAUNCH;
+  }
   mla::verify_split_kernel<<<static_cast<unsigned>(2 * units), mla::kThreads, kSmemBytes, stream>>>(
       map_qn, map_qr, map_kvs0, map_kvs1, map_kvo, map_out, p);
   if (cudaGetLastError() != cudaSuccess) return MLA_ERR_LAUNCH;
+  if (timing && cudaEventRecord(g_timing_after, stream) != cudaSuccess) {
+    cudaGetLastError();
+    return MLA_ERR_LAUNCH;
+  }
   if (ns > 1) {
     mla::CombineParams c;
     c.part_o = part_o;
@@ -304,12 +317,19 @@ int mla_verify_attn(const void* q_nope_abs, const void* q_rope, const void* kv,
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = timing ? 0 : 1;   // an event between the launches: plain ordering
     if (cudaLaunchKernelEx(&cfg, mla::combine_kernel, c) != cudaSuccess) {
       cudaGetLastError();
       return MLA_ERR_LAUNCH;
     }
   }
+  return MLA_OK;
+}
+
+int mla_verify_attn_set_timing_events(cudaEvent_t before_split, cudaEvent_t after_split) {
+  if ((before_split == nullptr) != (after_split == nullptr)) return MLA_ERR_NULLPTR;
+  g_timing_before = before_split;
+  g_timing_after = after_split;
   return MLA_OK;
 }
 
