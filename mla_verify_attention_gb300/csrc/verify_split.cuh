@@ -321,10 +321,46 @@ __device__ __forceinline__ void s_softmax(Smem& sm, const Unit& u, const SplitPa
   bool copy_failed = false;       // set by the copy-issuing thread only
   bool finished = true;
 
+  // Stage P (and the row sums) for 8 keys at a time into exchange buffer `xb`
+  // [alpha | flags | P hi | P lo] with exponent offset msub; returns the sum.
+  auto stage_p = [&](const uint32_t* sr, uint8_t* xb, float msub) -> float {
+    uint8_t* ph = xb + kPHead + r * 128;
+    // Exponent arguments and running sums in packed fp32 pairs.
+    const uint64_t a2 = f2pack(a_eff, a_eff);
+    const uint64_t m2 = f2pack(-msub, -msub);
+    uint64_t ls2[2] = {0ull, 0ull};                 // bit pattern 0 = (0.f, 0.f)
+#pragma unroll
+    for (int q4 = 0; q4 < 4; ++q4) {
+      const int unit = 4 * half + q4;               // 16-byte unit = keys 8*unit .. 8*unit+7
+      uint32_t h[4], lw[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int c = 4 * q4 + e;
+        float x0, x1;
+        f2unpack(ffma2(f2pack(__uint_as_float(sr[2 * c]), __uint_as_float(sr[2 * c + 1])), a2, m2),
+                 x0, x1);
+        const float p0 = ex2(x0);
+        const float p1 = ex2(x1);
+        ls2[e & 1] = fadd2(ls2[e & 1], f2pack(p0, p1));
+        h[e] = pack_bf16x2(p0, p1);
+        if (kTwoTerm) lw[e] = pack_bf16x2(p0 - bf16lo_to_f32(h[e]), p1 - bf16hi_to_f32(h[e]));
+      }
+      *reinterpret_cast<uint4*>(ph + ((unit ^ (r & 7)) << 4)) = make_uint4(h[0], h[1], h[2], h[3]);
+      if (kTwoTerm)
+        *reinterpret_cast<uint4*>(ph + kPTerm + ((unit ^ (r & 7)) << 4)) =
+            make_uint4(lw[0], lw[1], lw[2], lw[3]);
+    }
+    float s0, s1, s2, s3;
+    f2unpack(ls2[0], s0, s1);
+    f2unpack(ls2[1], s2, s3);
+    return (s0 + s1) + (s2 + s3);
+  };
+
   for (int j = 0; j < u.ntiles; ++j) {
     const int buf = j & 1;
     const bool got = warp_wait(sm, smem_u32(&sm.sfull[buf]), (j >> 1) & 1, p, 7);
     uint32_t sr[32];
+    float mh = -CUDART_INF_F;   // this half's tile max (log2-scaled)
     if (got) {
       tc_fence_after();
       MLA_TMEM_LD_32x32b_X32(tmem + lane_base + kQCols + 64 * buf + 32 * half, sr);
@@ -358,76 +394,59 @@ __device__ __forceinline__ void s_softmax(Smem& sm, const Unit& u, const SplitPa
       for (int k = 0; k < 4; ++k) mx[k] = __uint_as_float(sr[k]);
 #pragma unroll
       for (int c = 4; c < 32; ++c) mx[c & 3] = fmaxf(mx[c & 3], __uint_as_float(sr[c]));
-      sm.xmax[half][r] = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * a_eff;
+      mh = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * a_eff;
     }
-    if (named_bar_red_or(kSoftmaxBar, kRowThreads, !got || copy_failed)) {
-      finished = false;
-      break;
-    }
-    const float mt = fmaxf(sm.xmax[0][r], sm.xmax[1][r]);
     // Lazy rescale: P may exceed 1 by up to 2^kLazyRescale; O and l only get
-    // rescaled (here and in the O CTA) when the max grows beyond that.
-    float alpha = 1.f;
-    bool flag = false;
-    if (mt > m_used + kLazyRescale) {
-      alpha = ex2(m_used - mt);          // 0 when nothing was visible before
-      flag = (m_used != -CUDART_INF_F);  // an all-zero O row needs no rescale
-      m_used = mt;
-      l *= alpha;
-    }
-    const float msub = (m_used == -CUDART_INF_F) ? 0.f : m_used;
-
-    // P for 8 keys at a time, staged straight into buffer `buf` [alpha | flags
-    // | P hi | P lo]; one bulk copy then moves it into the O CTA.  The copy
-    // that last read this buffer (tile j-2) was waited for by its issuer
-    // before the barrier above.
+    // rescaled (here and in the O CTA) when the max grows beyond that.  Each
+    // half first assumes that neither half of its row needs that (the usual
+    // case once a few tiles are in) and stages P with the current max; the
+    // one barrier per tile tells whether any row of the tile overflowed.
+    const bool ovf = mh > m_used + kLazyRescale;
     uint8_t* xb = sm.ring + kPOffset + buf * kPBuf;
-    uint8_t* ph = xb + kPHead + r * 128;
-    // Exponent arguments and running sums in packed fp32 pairs.
-    const uint64_t a2 = f2pack(a_eff, a_eff);
-    const uint64_t m2 = f2pack(-msub, -msub);
-    uint64_t ls2[2] = {0ull, 0ull};                 // bit pattern 0 = (0.f, 0.f)
-#pragma unroll
-    for (int q4 = 0; q4 < 4; ++q4) {
-      const int unit = 4 * half + q4;               // 16-byte unit = keys 8*unit .. 8*unit+7
-      uint32_t h[4], lw[4];
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const int c = 4 * q4 + e;
-        float x0, x1;
-        f2unpack(ffma2(f2pack(__uint_as_float(sr[2 * c]), __uint_as_float(sr[2 * c + 1])), a2, m2),
-                 x0, x1);
-        const float p0 = ex2(x0);
-        const float p1 = ex2(x1);
-        ls2[e & 1] = fadd2(ls2[e & 1], f2pack(p0, p1));
-        h[e] = pack_bf16x2(p0, p1);
-        if (kTwoTerm) lw[e] = pack_bf16x2(p0 - bf16lo_to_f32(h[e]), p1 - bf16hi_to_f32(h[e]));
-      }
-      *reinterpret_cast<uint4*>(ph + ((unit ^ (r & 7)) << 4)) = make_uint4(h[0], h[1], h[2], h[3]);
-      if (kTwoTerm)
-        *reinterpret_cast<uint4*>(ph + kPTerm + ((unit ^ (r & 7)) << 4)) =
-            make_uint4(lw[0], lw[1], lw[2], lw[3]);
-    }
-    {
-      float s0, s1, s2, s3;
-      f2unpack(ls2[0], s0, s1);
-      f2unpack(ls2[1], s2, s3);
-      l += (s0 + s1) + (s2 + s3);
-    }
-    if (half == 0) {
-      reinterpret_cast<float*>(xb)[r] = alpha;
-      const uint32_t any = __any_sync(0xFFFFFFFFu, flag) ? 1u : 0u;
-      if (lane == 0) reinterpret_cast<uint32_t*>(xb + 512)[wq] = any;
-    }
+    // Buffer `buf` was last read by the copy of tile j-2, which its issuer
+    // saw completed before the previous tile's barrier.
+    float lsum = stage_p(sr, xb, m_used == -CUDART_INF_F ? 0.f : m_used);
+    if (half == 0 && lane == 0) reinterpret_cast<uint32_t*>(xb + 512)[wq] = 0u;
+    // The copy of tile j-1 must have read its buffer before anyone passes
+    // this barrier: tile j+1 reuses that buffer.
+    if (half == 0 && r == 0) bulk_wait_read<0>();
     fence_proxy_async_smem();
-    named_bar_sync(kSoftmaxBar, kRowThreads);
+    // One barrier per tile: any overflowing row, or any failed wait.  Only
+    // then (rarely) a second one tells the two apart.
+    if (named_bar_red_or(kSoftmaxBar, kRowThreads, ovf || !got || copy_failed)) {
+      if (named_bar_red_or(kSoftmaxBar, kRowThreads, !got || copy_failed)) {
+        finished = false;
+        break;
+      }
+      // Some row's max grew beyond the lazy bound: agree on the row max
+      // through shared memory, rescale, and stage P again.
+      sm.xmax[half][r] = mh;
+      named_bar_sync(kSoftmaxBar, kRowThreads);
+      const float mt = fmaxf(sm.xmax[0][r], sm.xmax[1][r]);
+      float alpha = 1.f;
+      bool flag = false;
+      if (mt > m_used + kLazyRescale) {
+        alpha = ex2(m_used - mt);          // 0 when nothing was visible before
+        flag = (m_used != -CUDART_INF_F);  // an all-zero O row needs no rescale
+        m_used = mt;
+        l *= alpha;
+      }
+      lsum = stage_p(sr, xb, m_used == -CUDART_INF_F ? 0.f : m_used);
+      if (half == 0) {
+        reinterpret_cast<float*>(xb)[r] = alpha;
+        const uint32_t fl = __any_sync(0xFFFFFFFFu, flag) ? 1u : 0u;
+        if (lane == 0) reinterpret_cast<uint32_t*>(xb + 512)[wq] = fl;
+      }
+      fence_proxy_async_smem();
+      named_bar_sync(kSoftmaxBar, kRowThreads);
+    }
+    l += lsum;
     if (half == 0 && r == 0) {
       // The O CTA's buffer `buf` is free once its PV product of tile j-2 is done.
       if (wait_or_abort<true>(sm, smem_u32(&sm.pempty[buf]), ((j >> 1) & 1) ^ 1, p, 8)) {
         bulk_copy_to_peer(xbuf0_remote + buf * kPBuf, xbuf0 + buf * kPBuf, xbytes,
                           buf ? pfull_remote1 : pfull_remote0);
         bulk_commit_group();
-        bulk_wait_read<1>();
       } else {
         copy_failed = true;
       }
