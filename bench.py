@@ -54,6 +54,9 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget-s", type=float, default=20.0)
     ap.add_argument("--e2e-steps", type=int, default=20)
+    ap.add_argument("--page-size", type=int, default=0,
+                    help="time the paged-cache entry point with pages of this many keys "
+                         "(a multiple of 64, pages in seeded random order); 0 = contiguous cache")
     return ap.parse_args()
 
 
@@ -227,6 +230,11 @@ def run_reference(args, rank):
     print(json.dumps(line), flush=True)
 
 
+def case_seed_for_pages(case):
+    """Seed of the page order of a bench case (fixed per workload shape)."""
+    return 0x5041 + int(case.Smax)
+
+
 def config_of(name, case, extra=None):
     w = I.WORKLOADS[name]
     c = {"workload": name, "B": case.B, "q_len": case.q, "H": case.H, "Dl": 512, "Dr": 64,
@@ -256,12 +264,20 @@ def run_ours(args, rank, world, local_rank):
     q_rope = t(case.q_rope.view(np.int16), torch.bfloat16)
     seq = t(case.seq_lens, torch.int32)
     mask = t(case.mask.view(np.int32), torch.int32)
-    kv0 = t(case.kv.view(np.int16), torch.bfloat16)
+    paged = args.page_size > 0
+    if paged:
+        pool, table = I.to_paged(case, args.page_size, seed=case_seed_for_pages(case), extra_pages=0)
+        kv0 = t(pool.view(np.int16), torch.bfloat16)
+        table_d = t(table, torch.int32)
+    else:
+        kv0 = t(case.kv.view(np.int16), torch.bfloat16)
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
     kv_bytes = kv0.numel() * 2
     copies = max(2, math.ceil(2.0 * l2 / kv_bytes) + 1)
     kvs = [kv0] + [kv0.clone() for _ in range(copies - 1)]
     B, q, H, Smax = case.B, case.q, case.H, case.Smax
+    if paged:
+        Smax = table.shape[1] * args.page_size      # the paged call's key bound
     out = torch.empty((B, q, H, 512), dtype=torch.float32, device=dev)
     lse = torch.empty((B, q, H), dtype=torch.float32, device=dev)
     need = mva.workspace_size(B, q, H, Smax)
@@ -273,9 +289,15 @@ def run_ours(args, rank, world, local_rank):
     ptrs = [q_nope.data_ptr(), q_rope.data_ptr(), None, seq.data_ptr(), mask.data_ptr()]
 
     def call(i):
-        st = mva.verify_attn_raw(ptrs[0], ptrs[1], kvs[i % copies].data_ptr(), ptrs[3], ptrs[4], B,
-                                 q, H, Smax, float(case.scale), out.data_ptr(), lse.data_ptr(),
-                                 ws.data_ptr(), ws.numel(), sh)
+        if paged:
+            st = mva.load_library().mla_verify_attn_paged(
+                ptrs[0], ptrs[1], kvs[i % copies].data_ptr(), kv0.shape[0], table_d.data_ptr(),
+                table_d.shape[1], args.page_size, ptrs[3], ptrs[4], B, q, H, float(case.scale),
+                out.data_ptr(), lse.data_ptr(), ws.data_ptr(), ws.numel(), sh)
+        else:
+            st = mva.verify_attn_raw(ptrs[0], ptrs[1], kvs[i % copies].data_ptr(), ptrs[3], ptrs[4],
+                                     B, q, H, Smax, float(case.scale), out.data_ptr(),
+                                     lse.data_ptr(), ws.data_ptr(), ws.numel(), sh)
         if st != 0:
             raise mva.MLAError(st)
 
@@ -337,8 +359,9 @@ def run_ours(args, rank, world, local_rank):
 
     # ---- end to end through the public API, from pinned host buffers
     host_in = [torch.from_numpy(np.ascontiguousarray(a)).pin_memory() for a in
-               (case.q_nope.view(np.int16), case.q_rope.view(np.int16), case.kv.view(np.int16),
-                case.seq_lens, case.mask.view(np.int32))]
+               (case.q_nope.view(np.int16), case.q_rope.view(np.int16),
+                (pool if paged else case.kv).view(np.int16), case.seq_lens, case.mask.view(np.int32))
+               + ((table,) if paged else ())]
     h_out = torch.empty((B, q, H, 512), dtype=torch.float32).pin_memory()
     h_lse = torch.empty((B, q, H), dtype=torch.float32).pin_memory()
     d_in = [torch.empty(h.shape, dtype=h.dtype, device=dev) for h in host_in]
@@ -348,9 +371,15 @@ def run_ours(args, rank, world, local_rank):
     def e2e_step():
         for d, h in zip(d_in, host_in):
             d.copy_(h, non_blocking=True)
-        o, l = mva.verify_attn(d_in[0].view(torch.bfloat16), d_in[1].view(torch.bfloat16),
-                               d_in[2].view(torch.bfloat16), d_in[3], d_in[4], float(case.scale),
-                               out=out, lse=lse, workspace=ws if need > 0 else None)
+        if paged:
+            o, l = mva.verify_attn_paged(d_in[0].view(torch.bfloat16), d_in[1].view(torch.bfloat16),
+                                         d_in[2].view(torch.bfloat16), d_in[5], args.page_size,
+                                         d_in[3], d_in[4], float(case.scale), out=out, lse=lse,
+                                         workspace=ws if need > 0 else None)
+        else:
+            o, l = mva.verify_attn(d_in[0].view(torch.bfloat16), d_in[1].view(torch.bfloat16),
+                                   d_in[2].view(torch.bfloat16), d_in[3], d_in[4], float(case.scale),
+                                   out=out, lse=lse, workspace=ws if need > 0 else None)
         h_out.copy_(o, non_blocking=True)
         h_lse.copy_(l, non_blocking=True)
 
@@ -409,6 +438,8 @@ def run_ours(args, rank, world, local_rank):
                 "l2": "inputs larger than L2: %d rotating cache copies (%.0f MB > %.0f MB L2)" % (
                     copies, copies * kv_bytes / 1e6, l2 / 1e6),
                 "plan": {"row_tiles": n_rt, "nsplit": nsplit, "chunk_tiles": chunk},
+                "cache": ("paged: %d-key pages in seeded random order" % args.page_size) if paged
+                else "contiguous [B, Smax, 576]",
                 "parallelism": "replicas" if world > 1 else "single GPU",
                 "vs_baseline_ref": ("pages' best sm_120 time for this workload: %.1f us "
                                     "(RTX PRO 6000, fp32), context only" % ref) if ref else None}),

@@ -59,7 +59,8 @@ enum mla_status {
   MLA_ERR_LAUNCH = -6,             /* a kernel launch or tensor-map creation failed */
   MLA_ERR_DEVICE_TIMEOUT = -7,     /* (device status) an internal pipeline wait gave up */
   MLA_ERR_SEQLEN = -8,             /* (device status) some seq_lens[b] outside [q_len, Smax] */
-  MLA_ERR_ARG = -9                 /* any other invalid argument (e.g. non-finite scale) */
+  MLA_ERR_ARG = -9,                /* any other invalid argument (e.g. non-finite scale) */
+  MLA_ERR_PAGE = -10               /* (device status) a block-table entry outside the page pool */
 };
 
 /*
@@ -105,8 +106,39 @@ int mla_verify_attn(const void* q_nope_abs, const void* q_rope, const void* kv,
                     size_t workspace_bytes, cudaStream_t stream);
 
 /*
+ * mla_verify_attn over a paged cache.  The pages have no paged interface; they
+ * name a paged cache (page_size 1, scattered rows) as the production layout
+ * (page "The Moment of Truth: Benchmarking a Custom sm_120 Flash Attention
+ * Kernel", section "Output Knowledge Created").  Pages of a multiple of 64 keys
+ * are supported here.  The computation is that of mla_verify_attn with
+ *   kv[b, t, :] = kv_pool[block_table[b, t / page_size] * page_size + t % page_size, :]
+ * i.e. key t of stream b lives in page block_table[b][t / page_size] of the pool.
+ *
+ *   kv_pool      [pool_rows, 576] bf16, rows = pages x page_size, 16-byte aligned.
+ *                Rows of pages no stream refers to, and rows past a stream's
+ *                seq_len, may hold anything (NaN included).
+ *   pool_rows    rows in the pool: a multiple of page_size, < 2^31.
+ *   block_table  [B, max_blocks] int32, 4-byte aligned: the page of each
+ *                page_size-key block; entries past ceil(seq_lens[b] / page_size)
+ *                are not read.  An entry outside [0, pool_rows / page_size) is
+ *                reported as MLA_ERR_PAGE through the device status (that
+ *                stream's results are then undefined).
+ *   max_blocks   blocks per stream in block_table; Smax = max_blocks * page_size
+ *                (< 2^24) bounds seq_lens[b] and sizes the workspace
+ *                (mla_verify_attn_workspace_size(B, q_len, H, Smax)).
+ *   page_size    keys per page: a positive multiple of 64 (a 64-key tile then
+ *                never crosses a page); otherwise MLA_ERR_SHAPE.
+ * All other arguments, results and errors as for mla_verify_attn.
+ */
+int mla_verify_attn_paged(const void* q_nope_abs, const void* q_rope, const void* kv_pool,
+                          long long pool_rows, const int32_t* block_table, int max_blocks,
+                          int page_size, const int32_t* seq_lens, const uint32_t* tree_mask, int B,
+                          int q_len, int H, float scale, float* out, float* lse, void* workspace,
+                          size_t workspace_bytes, cudaStream_t stream);
+
+/*
  * Synchronises `stream`, then returns and clears the current device's status
- * word: MLA_OK, MLA_ERR_SEQLEN or MLA_ERR_DEVICE_TIMEOUT (the first recorded),
+ * word: MLA_OK, MLA_ERR_SEQLEN, MLA_ERR_DEVICE_TIMEOUT or MLA_ERR_PAGE (the first recorded),
  * or MLA_ERR_LAUNCH if the synchronisation itself failed.  The word is shared
  * by all calls on the device since it was last read.
  */

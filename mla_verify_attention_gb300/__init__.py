@@ -5,8 +5,8 @@ The computation runs in hand-written CUDA kernels behind the C ABI declared in
 binds it with ctypes.  ``inputs`` makes seeded synthetic workloads.
 """
 from ._lib import (MLAError, last_device_error, load_library, plan, set_timing_events, strerror,
-                   verify_attn, verify_attn_raw, workspace_size)
+                   verify_attn, verify_attn_paged, verify_attn_raw, workspace_size)
 from ._build import build
 
 __all__ = ["MLAError", "build", "last_device_error", "load_library", "plan", "set_timing_events",
-           "strerror", "verify_attn", "verify_attn_raw", "workspace_size"]
+           "strerror", "verify_attn", "verify_attn_paged", "verify_attn_raw", "workspace_size"]

@@ -16,7 +16,7 @@ MLA_OK = 0
 STATUS_NAMES = {
     0: "MLA_OK", -1: "MLA_ERR_NULLPTR", -2: "MLA_ERR_SHAPE", -3: "MLA_ERR_ALIGN",
     -4: "MLA_ERR_WORKSPACE", -5: "MLA_ERR_UNSUPPORTED_DEVICE", -6: "MLA_ERR_LAUNCH",
-    -7: "MLA_ERR_DEVICE_TIMEOUT", -8: "MLA_ERR_SEQLEN", -9: "MLA_ERR_ARG",
+    -7: "MLA_ERR_DEVICE_TIMEOUT", -8: "MLA_ERR_SEQLEN", -9: "MLA_ERR_ARG", -10: "MLA_ERR_PAGE",
 }
 EXPORTED = ("mla_verify_attn", "mla_verify_attn_workspace_size", "mla_verify_attn_last_device_error",
             "mla_verify_attn_strerror", "mla_verify_attn_plan")
@@ -51,6 +51,9 @@ def load_library(build_if_missing: bool = True) -> ctypes.CDLL:
         IP = ctypes.POINTER(ctypes.c_int)
         lib.mla_verify_attn_plan.argtypes = [I, I, I, I, I, IP, IP, IP]
         lib.mla_verify_attn_plan.restype = I
+        L = ctypes.c_longlong
+        lib.mla_verify_attn_paged.argtypes = [P, P, P, L, P, I, I, P, P, I, I, I, F, P, P, P, Z, P]
+        lib.mla_verify_attn_paged.restype = I
         lib.mla_verify_attn_set_timing_events.argtypes = [P, P]
         lib.mla_verify_attn_set_timing_events.restype = I
         _lib = lib
@@ -128,6 +131,48 @@ def verify_attn(q_nope, q_rope, kv, seq_lens, tree_mask, scale, out=None, lse=No
                          lse.data_ptr(), ws_ptr, ws_bytes, _stream_handle(stream))
     if st != MLA_OK:
         raise MLAError(st)
+    return out, lse
+
+
+def verify_attn_paged(q_nope, q_rope, kv_pool, block_table, page_size, seq_lens, tree_mask, scale,
+                      out=None, lse=None, workspace=None, stream=None):
+    """verify_attn over a paged cache.
+
+    kv_pool [pool_rows, 576] bf16 (pages of page_size rows), block_table
+    [B, max_blocks] int32 (page of each page_size-key block of each stream),
+    page_size a positive multiple of 64; other arguments as for verify_attn.
+    """
+    import torch
+    B, q, H, Dl = q_nope.shape
+    pool_rows = kv_pool.shape[0]
+    max_blocks = block_table.shape[1]
+    if Dl != 512 or tuple(q_rope.shape) != (B, q, H, 64) or kv_pool.dim() != 2 or kv_pool.shape[1] != 576:
+        raise ValueError("expected q_nope [B,q,H,512], q_rope [B,q,H,64], kv_pool [rows,576]")
+    if tuple(block_table.shape) != (B, max_blocks):
+        raise ValueError("expected block_table [B, max_blocks]")
+    for name, t, dt in (("q_nope", q_nope, torch.bfloat16), ("q_rope", q_rope, torch.bfloat16),
+                        ("kv_pool", kv_pool, torch.bfloat16), ("seq_lens", seq_lens, torch.int32),
+                        ("block_table", block_table, torch.int32)):
+        if t.dtype != dt or not t.is_cuda or not t.is_contiguous():
+            raise ValueError("%s must be a contiguous CUDA %s tensor" % (name, dt))
+    if tree_mask.element_size() != 4 or not tree_mask.is_cuda or not tree_mask.is_contiguous():
+        raise ValueError("tree_mask must be a contiguous CUDA 32-bit tensor")
+    dev = q_nope.device
+    if out is None:
+        out = torch.empty((B, q, H, 512), dtype=torch.float32, device=dev)
+    if lse is None:
+        lse = torch.empty((B, q, H), dtype=torch.float32, device=dev)
+    need = workspace_size(B, q, H, max_blocks * page_size)
+    if workspace is None and need > 0:
+        workspace = torch.empty(need, dtype=torch.uint8, device=dev)
+    ws_ptr = workspace.data_ptr() if workspace is not None else 0
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    st = int(load_library().mla_verify_attn_paged(
+        q_nope.data_ptr(), q_rope.data_ptr(), kv_pool.data_ptr(), pool_rows, block_table.data_ptr(),
+        max_blocks, int(page_size), seq_lens.data_ptr(), tree_mask.data_ptr(), B, q, H, float(scale),
+        out.data_ptr(), lse.data_ptr(), ws_ptr, ws_bytes, _stream_handle(stream)))
+    if st != MLA_OK:
+        raise MLAError(st, "mla_verify_attn_paged")
     return out, lse
 
 

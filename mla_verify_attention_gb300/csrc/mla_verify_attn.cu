@@ -164,6 +164,7 @@ const char* mla_verify_attn_strerror(int status) {
     case MLA_ERR_WORKSPACE: return "MLA_ERR_WORKSPACE: workspace smaller than required";
     case MLA_ERR_UNSUPPORTED_DEVICE: return "MLA_ERR_UNSUPPORTED_DEVICE: current device is not sm_103";
     case MLA_ERR_LAUNCH: return "MLA_ERR_LAUNCH: kernel launch or tensor-map creation failed";
+    case MLA_ERR_PAGE: return "MLA_ERR_PAGE: a block-table entry outside the page pool";
     case MLA_ERR_DEVICE_TIMEOUT: return "MLA_ERR_DEVICE_TIMEOUT: a device pipeline wait gave up";
     case MLA_ERR_SEQLEN: return "MLA_ERR_SEQLEN: seq_lens[b] outside [q_len, Smax]";
     case MLA_ERR_ARG: return "MLA_ERR_ARG: invalid argument";
@@ -193,10 +194,43 @@ size_t mla_verify_attn_workspace_size(int B, int q_len, int H, int Smax) {
   return workspace_bytes_for(B, q_len, H, ns);
 }
 
-int mla_verify_attn(const void* q_nope_abs, const void* q_rope, const void* kv,
-                    const int32_t* seq_lens, const uint32_t* tree_mask, int B, int q_len, int H,
-                    int Smax, float scale, float* out, float* lse, void* workspace,
-                    size_t workspace_bytes, cudaStream_t stream) {
+}  // extern "C"
+
+namespace {
+
+// One verify call: a contiguous cache (block_table == nullptr) or a paged one.
+struct Call {
+  const void* q_nope_abs;
+  const void* q_rope;
+  const void* kv;                 // [B][Smax][576] or the page pool [pool_rows][576]
+  const int32_t* seq_lens;
+  const uint32_t* tree_mask;
+  int B, q_len, H, Smax;
+  float scale;
+  float* out;
+  float* lse;
+  void* workspace;
+  size_t workspace_bytes;
+  cudaStream_t stream;
+  const int32_t* block_table;     // paged: [B][max_blocks]
+  int max_blocks, page_size;
+  long long pool_rows;
+};
+
+int run(const Call& c) {
+  const void* q_nope_abs = c.q_nope_abs;
+  const void* q_rope = c.q_rope;
+  const void* kv = c.kv;
+  const int32_t* seq_lens = c.seq_lens;
+  const uint32_t* tree_mask = c.tree_mask;
+  const int B = c.B, q_len = c.q_len, H = c.H, Smax = c.Smax;
+  const float scale = c.scale;
+  float* out = c.out;
+  float* lse = c.lse;
+  void* workspace = c.workspace;
+  const size_t workspace_bytes = c.workspace_bytes;
+  cudaStream_t stream = c.stream;
+  const bool paged = c.block_table != nullptr;
   if (!shape_ok(B, q_len, H, Smax)) return MLA_ERR_SHAPE;
   if (!std::isfinite(scale)) return MLA_ERR_ARG;
   if (B == 0) return MLA_OK;
@@ -235,8 +269,10 @@ int mla_verify_attn(const void* q_nope_abs, const void* q_rope, const void* kv,
     if (encode(d, &map_qr, q_rope, 2, dims, strides, box) != MLA_OK) return MLA_ERR_LAUNCH;
   }
   {
-    const cuuint64_t dims[4] = {64, static_cast<cuuint64_t>(Smax), 9, static_cast<cuuint64_t>(B)};
-    const cuuint64_t strides[3] = {576 * 2, 64 * 2, static_cast<cuuint64_t>(Smax) * 576 * 2};
+    // Rows of the cache: [B][Smax] (contiguous) or the page pool (paged, one "stream").
+    const cuuint64_t nrow = paged ? static_cast<cuuint64_t>(c.pool_rows) : static_cast<cuuint64_t>(Smax);
+    const cuuint64_t dims[4] = {64, nrow, 9, static_cast<cuuint64_t>(paged ? 1 : B)};
+    const cuuint64_t strides[3] = {576 * 2, 64 * 2, nrow * 576 * 2};
     // S CTA: a key tile's chunks 0..4 and 5..8 as two boxes; O CTA: chunks 0..7.
     const cuuint32_t box_s0[4] = {64, mla::kKeys, mla::kKSplit, 1};
     const cuuint32_t box_s1[4] = {64, mla::kKeys, 9 - mla::kKSplit, 1};
@@ -278,6 +314,10 @@ int mla_verify_attn(const void* q_nope_abs, const void* q_rope, const void* kv,
   p.chunk_tiles = ct;
   p.two_term_max_keys = kTwoTermMaxKeys;
   p.scale_log2 = scale * 1.4426950408889634f;
+  p.block_table = c.block_table;
+  p.max_blocks = paged ? c.max_blocks : 0;
+  p.page_size = paged ? c.page_size : 0;
+  p.pool_pages = paged ? static_cast<int>(c.pool_rows / c.page_size) : 0;
 
   const long long units = static_cast<long long>(B) * nrt * ns;
   if (2 * units >= (1LL << 31)) return MLA_ERR_SHAPE;
@@ -326,6 +366,36 @@ int mla_verify_attn(const void* q_nope_abs, const void* q_rope, const void* kv,
   return MLA_OK;
 }
 
+}  // namespace
+
+extern "C" {
+
+int mla_verify_attn(const void* q_nope_abs, const void* q_rope, const void* kv,
+                    const int32_t* seq_lens, const uint32_t* tree_mask, int B, int q_len, int H,
+                    int Smax, float scale, float* out, float* lse, void* workspace,
+                    size_t workspace_bytes, cudaStream_t stream) {
+  Call c{q_nope_abs, q_rope, kv, seq_lens, tree_mask, B, q_len, H, Smax, scale, out, lse,
+         workspace, workspace_bytes, stream, nullptr, 0, 0, 0};
+  return run(c);
+}
+
+int mla_verify_attn_paged(const void* q_nope_abs, const void* q_rope, const void* kv_pool,
+                          long long pool_rows, const int32_t* block_table, int max_blocks,
+                          int page_size, const int32_t* seq_lens, const uint32_t* tree_mask, int B,
+                          int q_len, int H, float scale, float* out, float* lse, void* workspace,
+                          size_t workspace_bytes, cudaStream_t stream) {
+  if (page_size < mla::kKeys || page_size % mla::kKeys != 0 || max_blocks < 1 || pool_rows < 1 ||
+      pool_rows % page_size != 0 || pool_rows >= (1LL << 31) ||
+      static_cast<long long>(max_blocks) * page_size >= (1LL << 24))
+    return MLA_ERR_SHAPE;
+  if (B > 0 && (!block_table || !kv_pool)) return MLA_ERR_NULLPTR;
+  if (block_table && !aligned(block_table, 4)) return MLA_ERR_ALIGN;
+  Call c{q_nope_abs, q_rope, kv_pool, seq_lens, tree_mask, B, q_len, H, max_blocks * page_size,
+         scale, out, lse, workspace, workspace_bytes, stream, block_table, max_blocks, page_size,
+         pool_rows};
+  return run(c);
+}
+
 int mla_verify_attn_set_timing_events(cudaEvent_t before_split, cudaEvent_t after_split) {
   if ((before_split == nullptr) != (after_split == nullptr)) return MLA_ERR_NULLPTR;
   g_timing_before = before_split;
@@ -348,6 +418,7 @@ int mla_verify_attn_last_device_error(cudaStream_t stream) {
     return MLA_ERR_LAUNCH;
   if (v & mla::kStatusSeqLen) return MLA_ERR_SEQLEN;
   if (v & mla::kStatusTimeout) return MLA_ERR_DEVICE_TIMEOUT;
+  if (v & mla::kStatusPage) return MLA_ERR_PAGE;
   return MLA_OK;
 }
 

@@ -83,7 +83,7 @@ constexpr uint32_t kIdescPV = idesc_bf16_f32(128, 256, 0, 1);
 enum : uint32_t { kCmdDone = 0xFFFFFFFFu, kCmdZeroTail = 0x80000000u };
 
 // Device status bits (first error wins in the host's report).
-enum : uint32_t { kStatusSeqLen = 1u, kStatusTimeout = 2u };
+enum : uint32_t { kStatusSeqLen = 1u, kStatusTimeout = 2u, kStatusPage = 4u };
 
 struct SplitParams {
   const int32_t* seq_lens;
@@ -95,6 +95,11 @@ struct SplitParams {
   int n_rt, nsplit, chunk_tiles;
   int two_term_max_keys;
   float scale_log2;   // scale * log2(e)
+  // Paged cache (null block_table: contiguous [B][Smax][576] cache).  Key k of
+  // stream b is row block_table[b][k / page_size] * page_size + k % page_size of
+  // the page pool; page_size is a multiple of 64, so no key tile crosses a page.
+  const int32_t* block_table;   // [B][max_blocks]
+  int max_blocks, page_size, pool_pages;
 };
 
 struct __align__(1024) Smem {
@@ -142,6 +147,20 @@ __device__ __forceinline__ Unit decode_unit(const SplitParams& p) {
   u.two_term = u.S <= p.two_term_max_keys;
   u.zero_tail = !u.empty && ((u.k1 - u.k0) % kKeys) != 0;
   return u;
+}
+
+// TMA coordinates (row, stream) of the first key of a 64-key tile: the key
+// within stream b of the contiguous cache, or the row of the page pool.  A
+// block-table entry outside the pool is reported and replaced by page 0.
+__device__ __forceinline__ int2 tile_origin(const SplitParams& p, const Unit& u, int key) {
+  if (p.block_table == nullptr) return make_int2(key, u.b);
+  const int blk = key / p.page_size;
+  int page = __ldg(p.block_table + static_cast<size_t>(u.b) * p.max_blocks + blk);
+  if (page < 0 || page >= p.pool_pages) {
+    atomicOr(p.status, kStatusPage);
+    page = 0;
+  }
+  return make_int2(page * p.page_size + (key - blk * p.page_size), 0);
 }
 
 // Bounded wait that also gives up as soon as another warp of the CTA aborted.
@@ -209,7 +228,13 @@ __device__ __forceinline__ void s_producer(Smem& sm, const Unit& u, const SplitP
   // Two boxes per 64-key tile: [5 chunks][64 keys][64 dims] and [4 chunks][64][64].
   // A part's buffer is refilled as soon as the MMAs that read it are done, so
   // the first chunks of tile j+2 load while the last ones of tile j are used.
+  // Tile origins are looked up two tiles ahead (a block-table read for paged caches).
+  int2 org0 = tile_origin(p, u, u.k0);
+  int2 org1 = u.ntiles > 1 ? tile_origin(p, u, u.k0 + kKeys) : org0;
   for (int j = 0; j < u.ntiles; ++j) {
+    const int2 org = org0;
+    org0 = org1;
+    if (j + 2 < u.ntiles) org1 = tile_origin(p, u, u.k0 + (j + 2) * kKeys);
     const int slot = j % kKSlots;
 #pragma unroll
     for (int part = 0; part < 2; ++part) {
@@ -217,8 +242,8 @@ __device__ __forceinline__ void s_producer(Smem& sm, const Unit& u, const SplitP
         return;
       const uint32_t full = smem_u32(&sm.kfull[part][slot]);
       mbar_arrive_expect_tx(full, part ? kKPart1 : kKPart0);
-      tma_load_4d(ring + slot * kKTile + part * kKPart0, part ? map_kv1 : map_kv0, 0,
-                  u.k0 + j * kKeys, part ? kKSplit : 0, u.b, full);
+      tma_load_4d(ring + slot * kKTile + part * kKPart0, part ? map_kv1 : map_kv0, 0, org.x,
+                  part ? kKSplit : 0, org.y, full);
       n_issued[part] = j + 1;
     }
   }
@@ -466,12 +491,17 @@ __device__ __forceinline__ void s_softmax(Smem& sm, const Unit& u, const SplitPa
 __device__ __forceinline__ void o_producer(Smem& sm, const Unit& u, const SplitParams& p,
                                            const CUtensorMap* map_kv, int& n_issued) {
   const uint32_t ring = smem_u32(sm.ring);
+  int2 org0 = tile_origin(p, u, u.k0);
+  int2 org1 = u.ntiles > 1 ? tile_origin(p, u, u.k0 + kKeys) : org0;
   for (int j = 0; j < u.ntiles; ++j) {
+    const int2 org = org0;
+    org0 = org1;
+    if (j + 2 < u.ntiles) org1 = tile_origin(p, u, u.k0 + (j + 2) * kKeys);
     const int slot = j & 1;
     if (!wait_or_abort(sm, smem_u32(&sm.vempty[slot]), ((j >> 1) & 1) ^ 1, p, 9)) return;
     const uint32_t full = smem_u32(&sm.vfull[slot]);
     mbar_arrive_expect_tx(full, kVTile);
-    tma_load_4d(ring + slot * kVTile, map_kv, 0, u.k0 + j * kKeys, 0, u.b, full);
+    tma_load_4d(ring + slot * kVTile, map_kv, 0, org.x, 0, org.y, full);
     n_issued = j + 1;
   }
 }

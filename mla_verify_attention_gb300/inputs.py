@@ -256,6 +256,30 @@ def default_scale() -> np.float32:
     return np.float32(1.0 / math.sqrt(192.0))
 
 
+def to_paged(case: "Case", page_size: int, seed: int, extra_pages: int = 3):
+    """Lay a case's cache out as a page pool for the paged entry point.
+
+    Each stream's keys 0 .. max_blocks*page_size-1 are cut into blocks of
+    page_size rows and placed at pages given by a seeded random permutation of
+    the pool (which has ``extra_pages`` pages no stream uses).  Rows of the
+    logical cache past Smax, and unused pages, are NaN.  Returns
+    (kv_pool [pool_rows, 576] uint16, block_table [B, max_blocks] int32).
+    """
+    B, Smax, D = case.kv.shape
+    max_blocks = -(-Smax // page_size)
+    pages = B * max_blocks + extra_pages
+    order = np.argsort(uniform(seed, "pages", pages), kind="stable").astype(np.int32)
+    table = order[: B * max_blocks].reshape(B, max_blocks)
+    pool = np.full((pages * page_size, D), 0x7FC0, dtype=np.uint16)
+    for b in range(B):
+        for k in range(max_blocks):
+            lo, hi = k * page_size, min((k + 1) * page_size, Smax)
+            if lo < hi:
+                dst = int(table[b, k]) * page_size
+                pool[dst:dst + hi - lo] = case.kv[b, lo:hi]
+    return pool, np.ascontiguousarray(table)
+
+
 def make_case(w: Workload, seed: int | None = None, pad: str = "nan",
               smax_align: int = 64, prefixes=None) -> Case:
     """Materialise a workload.

@@ -89,3 +89,37 @@ def test_plan_env_override(lib, monkeypatch):
     assert mva.plan(1, 9, 64, 320, 76) == (5, 3, 2)
     monkeypatch.setenv("MLA_VERIFY_NSPLIT", "100")
     assert mva.plan(1, 9, 64, 320, 76) == (5, 5, 1)
+
+
+def paged(lib, **kw):
+    a = dict(qn=16, qr=16, pool=16, rows=640, bt=16, mb=5, ps=128, sl=16, m=16, B=1, q=9, H=64,
+             scale=0.07, out=16, lse=16, ws=0, wsb=0)
+    a.update(kw)
+    return lib.mla_verify_attn_paged(a["qn"], a["qr"], a["pool"], a["rows"], a["bt"], a["mb"],
+                                     a["ps"], a["sl"], a["m"], a["B"], a["q"], a["H"], a["scale"],
+                                     a["out"], a["lse"], a["ws"], a["wsb"], None)
+
+
+def test_paged_host_argument_checks(lib):
+    # page sizes: positive multiples of 64 only; the pool is whole pages, < 2^31 rows
+    for ps in (0, 32, 100, -64):
+        assert paged(lib, ps=ps) == -2, ps
+    assert paged(lib, rows=650) == -2 and paged(lib, rows=0) == -2 and paged(lib, mb=0) == -2
+    assert paged(lib, rows=1 << 31) == -2
+    assert paged(lib, mb=1 << 18, ps=64) == -2                  # Smax = 2^24
+    assert paged(lib, bt=0) == -1 and paged(lib, pool=0) == -1
+    assert paged(lib, bt=2) == -3
+    assert paged(lib, B=0, bt=0, pool=0) == 0                   # nothing to do
+    assert paged(lib, q=0) == -2 and paged(lib, scale=float("nan")) == -9
+
+
+def test_paged_layout_helper():
+    from mla_verify_attention_gb300 import inputs as I
+    case = I.make_case(I.Workload("t", 2, 3, 100, "chain", H=2), smax_align=64)
+    pool, table = I.to_paged(case, 64, seed=5)
+    assert table.shape == (2, 2) and pool.shape == ((2 * 2 + 3) * 64, 576)
+    assert len(set(table.ravel().tolist())) == table.size        # distinct pages
+    for b in range(2):
+        for t in (0, 63, 64, int(case.seq_lens[b]) - 1):
+            row = int(table[b, t // 64]) * 64 + t % 64
+            assert (pool[row] == case.kv[b, t]).all()

@@ -1,0 +1,92 @@
+"""The paged-cache entry point (mla_verify_attn_paged) through the C ABI.
+
+Each case lays a seeded cache out as a page pool (random page order, NaN in
+unused pages and past each stream's length) and compares the paged call with
+the oracle on the logical cache, at the same tolerances as the contiguous
+path; one case also checks that paged and contiguous calls agree bit for bit.
+"""
+import numpy as np
+import pytest
+
+import oracle
+from mla_verify_attention_gb300 import inputs as I
+
+pytestmark = pytest.mark.gpu
+
+TOL_OUT = 2e-3
+TOL_LSE = 1e-3
+
+
+def _t(a, dt):
+    import torch
+    return torch.from_numpy(np.ascontiguousarray(a)).view(dt).cuda()
+
+
+def run_paged(case, page_size, seed=11, extra_pages=3):
+    import torch
+    import mla_verify_attention_gb300 as mva
+    pool, table = I.to_paged(case, page_size, seed, extra_pages)
+    out, lse = mva.verify_attn_paged(
+        _t(case.q_nope.view(np.int16), torch.bfloat16), _t(case.q_rope.view(np.int16), torch.bfloat16),
+        _t(pool.view(np.int16), torch.bfloat16), _t(table, torch.int32), page_size,
+        _t(case.seq_lens, torch.int32), _t(case.mask.view(np.int32), torch.int32), float(case.scale))
+    torch.cuda.synchronize()
+    st = mva.last_device_error()
+    assert st == 0, mva.strerror(st)
+    return out, lse
+
+
+def check(case, out, lse):
+    ref_out, ref_lse = oracle.case_reference(case)
+    o = out.cpu().numpy().astype(np.float64).reshape(ref_out.shape)
+    l = lse.cpu().numpy().astype(np.float64).reshape(ref_lse.shape)
+    empty = np.isneginf(ref_lse)
+    assert np.array_equal(np.isneginf(l), empty)
+    assert np.isfinite(o).all()
+    assert np.abs(o - ref_out).max() <= TOL_OUT
+    assert np.abs(l[~empty] - ref_lse[~empty]).max() <= TOL_LSE
+
+
+@pytest.mark.parametrize("B,q,H,prefixes,page_size", [
+    (1, 9, 64, [4096], 64),            # split path, one tile per page
+    (1, 9, 64, [700], 256),            # tiles inside larger pages, partial last page
+    (3, 5, 8, [10, 900, 2000], 128),   # ragged streams
+    (2, 33, 64, [300, 1500], 64),      # two mask words
+])
+def test_paged_matches_oracle(B, q, H, prefixes, page_size):
+    w = I.Workload("paged", B, q, 0, "random", 5, None, H=H)
+    case = I.make_case(w, seed=123 + B + q + page_size, prefixes=prefixes)
+    out, lse = run_paged(case, page_size)
+    check(case, out, lse)
+
+
+def test_paged_equals_contiguous_bitwise():
+    import torch
+    import mla_verify_attention_gb300 as mva
+    case = I.make_case(I.WORKLOADS["tree9_p4096"])
+    out_p, lse_p = run_paged(case, 64)
+    ref = mva.verify_attn(_t(case.q_nope.view(np.int16), torch.bfloat16),
+                          _t(case.q_rope.view(np.int16), torch.bfloat16),
+                          _t(case.kv.view(np.int16), torch.bfloat16), _t(case.seq_lens, torch.int32),
+                          _t(case.mask.view(np.int32), torch.int32), float(case.scale))
+    torch.cuda.synchronize()
+    # Smax is a whole number of 64-key pages, so both calls use the same split
+    # plan and the same arithmetic order.
+    assert case.Smax % 64 == 0
+    assert torch.equal(out_p, ref[0]) and torch.equal(lse_p, ref[1])
+
+
+def test_paged_bad_block_entry_is_reported():
+    import torch
+    import mla_verify_attention_gb300 as mva
+    case = I.make_case(I.WORKLOADS["chain9_p256"])
+    pool, table = I.to_paged(case, 64, seed=3)
+    table = table.copy()
+    table[0, 1] = pool.shape[0] // 64          # one past the last page
+    out, lse = mva.verify_attn_paged(
+        _t(case.q_nope.view(np.int16), torch.bfloat16), _t(case.q_rope.view(np.int16), torch.bfloat16),
+        _t(pool.view(np.int16), torch.bfloat16), _t(table, torch.int32), 64,
+        _t(case.seq_lens, torch.int32), _t(case.mask.view(np.int32), torch.int32), float(case.scale))
+    torch.cuda.synchronize()
+    assert mva.last_device_error() == -10          # MLA_ERR_PAGE, then cleared
+    assert mva.last_device_error() == 0
