@@ -110,7 +110,8 @@ int mla_verify_attn(const void* q_nope_abs, const void* q_rope, const void* kv,
  * name a paged cache (page_size 1, scattered rows) as the production layout
  * (page "The Moment of Truth: Benchmarking a Custom sm_120 Flash Attention
  * Kernel", section "Output Knowledge Created").  Pages of a multiple of 64 keys
- * are supported here.  The computation is that of mla_verify_attn with
+ * keep whole-tile TMA loads; any other page size (1 included) gathers rows
+ * with 16-byte cp.async copies.  The computation is that of mla_verify_attn with
  *   kv[b, t, :] = kv_pool[block_table[b, t / page_size] * page_size + t % page_size, :]
  * i.e. key t of stream b lives in page block_table[b][t / page_size] of the pool.
  *
@@ -126,8 +127,8 @@ int mla_verify_attn(const void* q_nope_abs, const void* q_rope, const void* kv,
  *   max_blocks   blocks per stream in block_table; Smax = max_blocks * page_size
  *                (< 2^24) bounds seq_lens[b] and sizes the workspace
  *                (mla_verify_attn_workspace_size(B, q_len, H, Smax)).
- *   page_size    keys per page: a positive multiple of 64 (a 64-key tile then
- *                never crosses a page); otherwise MLA_ERR_SHAPE.
+ *   page_size    keys per page, >= 1 (MLA_ERR_SHAPE otherwise).  Multiples of 64
+ *                are the fast path: a 64-key tile then never crosses a page.
  * All other arguments, results and errors as for mla_verify_attn.
  */
 int mla_verify_attn_paged(const void* q_nope_abs, const void* q_rope, const void* kv_pool,

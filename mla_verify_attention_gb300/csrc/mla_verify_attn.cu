@@ -70,8 +70,12 @@ int device_info(DeviceInfo** out) {
         d.status = MLA_ERR_UNSUPPORTED_DEVICE;
       d.encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
       if (d.status == MLA_OK &&
-          cudaFuncSetAttribute(mla::verify_split_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               static_cast<int>(kSmemBytes)) != cudaSuccess)
+          (cudaFuncSetAttribute(mla::verify_split_kernel<false>,
+                                cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                static_cast<int>(kSmemBytes)) != cudaSuccess ||
+           cudaFuncSetAttribute(mla::verify_split_kernel<true>,
+                                cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                static_cast<int>(kSmemBytes)) != cudaSuccess))
         d.status = MLA_ERR_LAUNCH;
       if (d.status == MLA_OK) {
         cudaLaunchConfig_t cfg = {};
@@ -79,7 +83,7 @@ int device_info(DeviceInfo** out) {
         cfg.blockDim = dim3(mla::kThreads, 1, 1);
         cfg.dynamicSmemBytes = kSmemBytes;
         int n = 0;
-        if (cudaOccupancyMaxActiveClusters(&n, mla::verify_split_kernel, &cfg) != cudaSuccess ||
+        if (cudaOccupancyMaxActiveClusters(&n, mla::verify_split_kernel<false>, &cfg) != cudaSuccess ||
             n < 1)
           n = sms / 2;
         d.max_clusters = n;
@@ -318,6 +322,9 @@ int run(const Call& c) {
   p.max_blocks = paged ? c.max_blocks : 0;
   p.page_size = paged ? c.page_size : 0;
   p.pool_pages = paged ? static_cast<int>(c.pool_rows / c.page_size) : 0;
+  // Pages that are not whole 64-key tiles: the kernel that gathers rows with cp.async.
+  const bool gather = paged && c.page_size % mla::kKeys != 0;
+  p.kv_pool = static_cast<const uint8_t*>(kv);
 
   const long long units = static_cast<long long>(B) * nrt * ns;
   if (2 * units >= (1LL << 31)) return MLA_ERR_SHAPE;
@@ -326,8 +333,12 @@ int run(const Call& c) {
     cudaGetLastError();
     return MLA_ERR_LAUNCH;
   }
-  mla::verify_split_kernel<<<static_cast<unsigned>(2 * units), mla::kThreads, kSmemBytes, stream>>>(
-      map_qn, map_qr, map_kvs0, map_kvs1, map_kvo, map_out, p);
+  if (gather)
+    mla::verify_split_kernel<true><<<static_cast<unsigned>(2 * units), mla::kThreads, kSmemBytes,
+                                     stream>>>(map_qn, map_qr, map_kvs0, map_kvs1, map_kvo, map_out, p);
+  else
+    mla::verify_split_kernel<false><<<static_cast<unsigned>(2 * units), mla::kThreads, kSmemBytes,
+                                      stream>>>(map_qn, map_qr, map_kvs0, map_kvs1, map_kvo, map_out, p);
   if (cudaGetLastError() != cudaSuccess) return MLA_ERR_LAUNCH;
   if (timing && cudaEventRecord(g_timing_after, stream) != cudaSuccess) {
     cudaGetLastError();
@@ -384,7 +395,7 @@ int mla_verify_attn_paged(const void* q_nope_abs, const void* q_rope, const void
                           int page_size, const int32_t* seq_lens, const uint32_t* tree_mask, int B,
                           int q_len, int H, float scale, float* out, float* lse, void* workspace,
                           size_t workspace_bytes, cudaStream_t stream) {
-  if (page_size < mla::kKeys || page_size % mla::kKeys != 0 || max_blocks < 1 || pool_rows < 1 ||
+  if (page_size < 1 || max_blocks < 1 || pool_rows < 1 ||
       pool_rows % page_size != 0 || pool_rows >= (1LL << 31) ||
       static_cast<long long>(max_blocks) * page_size >= (1LL << 24))
     return MLA_ERR_SHAPE;

@@ -101,10 +101,11 @@ def paged(lib, **kw):
 
 
 def test_paged_host_argument_checks(lib):
-    # page sizes: positive multiples of 64 only; the pool is whole pages, < 2^31 rows
-    for ps in (0, 32, 100, -64):
+    # page sizes >= 1; the pool is whole pages, < 2^31 rows
+    for ps in (0, -64):
         assert paged(lib, ps=ps) == -2, ps
     assert paged(lib, rows=650) == -2 and paged(lib, rows=0) == -2 and paged(lib, mb=0) == -2
+    assert paged(lib, ps=100, rows=750) == -2                  # 750 rows: not whole pages
     assert paged(lib, rows=1 << 31) == -2
     assert paged(lib, mb=1 << 18, ps=64) == -2                  # Smax = 2^24
     assert paged(lib, bt=0) == -1 and paged(lib, pool=0) == -1

@@ -4,6 +4,7 @@ Each case lays a seeded cache out as a page pool (random page order, NaN in
 unused pages and past each stream's length) and compares the paged call with
 the oracle on the logical cache, at the same tolerances as the contiguous
 path; one case also checks that paged and contiguous calls agree bit for bit.
+Pages of a multiple of 64 keys take the TMA path, other sizes the row gather.
 """
 import numpy as np
 import pytest
@@ -52,6 +53,10 @@ def check(case, out, lse):
     (1, 9, 64, [700], 256),            # tiles inside larger pages, partial last page
     (3, 5, 8, [10, 900, 2000], 128),   # ragged streams
     (2, 33, 64, [300, 1500], 64),      # two mask words
+    # page sizes that are not whole key tiles: rows gathered with cp.async
+    (1, 9, 64, [4096], 1),             # one row per page (scattered rows), split path
+    (3, 5, 8, [10, 900, 2000], 16),    # ragged streams, 16-row pages
+    (1, 33, 64, [700], 96),            # pages straddling key tiles
 ])
 def test_paged_matches_oracle(B, q, H, prefixes, page_size):
     w = I.Workload("paged", B, q, 0, "random", 5, None, H=H)
@@ -90,3 +95,18 @@ def test_paged_bad_block_entry_is_reported():
     torch.cuda.synchronize()
     assert mva.last_device_error() == -10          # MLA_ERR_PAGE, then cleared
     assert mva.last_device_error() == 0
+
+
+def test_gathered_pages_equal_contiguous_bitwise():
+    """Page size 1: the gather fills the same tile layout, so the result is the
+    contiguous call's, bit for bit."""
+    import torch
+    import mla_verify_attention_gb300 as mva
+    case = I.make_case(I.WORKLOADS["tree9_p4096"])
+    out_p, lse_p = run_paged(case, 1)
+    ref = mva.verify_attn(_t(case.q_nope.view(np.int16), torch.bfloat16),
+                          _t(case.q_rope.view(np.int16), torch.bfloat16),
+                          _t(case.kv.view(np.int16), torch.bfloat16), _t(case.seq_lens, torch.int32),
+                          _t(case.mask.view(np.int32), torch.int32), float(case.scale))
+    torch.cuda.synchronize()
+    assert torch.equal(out_p, ref[0]) and torch.equal(lse_p, ref[1])
