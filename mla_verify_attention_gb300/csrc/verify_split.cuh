@@ -136,11 +136,14 @@ struct Unit {
 
 __device__ __forceinline__ Unit decode_unit(const SplitParams& p) {
   Unit u;
+  // Units are numbered slice-major (all streams' slice 0, then slice 1, ...):
+  // clusters start in index order, so full-length slices go first and the
+  // shorter last slices of streams (and empty ones past a stream's end) last.
   const int unit = blockIdx.x >> 1;
   u.rt = unit % p.n_rt;
   const int t = unit / p.n_rt;
-  u.sp = t % p.nsplit;
-  u.b = t / p.nsplit;
+  u.b = t % p.B;
+  u.sp = t / p.B;
   u.S = p.seq_lens[u.b];
   u.prefix = u.S - p.q;
   u.rows_total = p.q * p.H;
