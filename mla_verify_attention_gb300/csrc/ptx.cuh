@@ -56,11 +56,6 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t byt
                : "memory");
 }
 
-// Arrive on an mbarrier of another CTA in the cluster (address from mapa).
-__device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_bar) {
-  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_bar)
-               : "memory");
-}
 
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   uint32_t ok;
@@ -139,23 +134,7 @@ __device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap* map
       : "memory");
 }
 
-// ---------------------------------------------------------------- DSMEM
-// Asynchronous 16-byte store into another CTA's shared memory; completion is
-// counted (in bytes) on that CTA's mbarrier.
-__device__ __forceinline__ void st_async_v4(uint32_t cluster_addr, uint4 v, uint32_t cluster_bar) {
-  asm volatile(
-      "st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.b32 [%0], {%1, %2, %3, %4}, [%5];"
-      ::"r"(cluster_addr), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w), "r"(cluster_bar)
-      : "memory");
-}
 
-__device__ __forceinline__ void st_async_b32(uint32_t cluster_addr, uint32_t v,
-                                             uint32_t cluster_bar) {
-  asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.b32 [%0], %1, [%2];" ::"r"(
-                   cluster_addr),
-               "r"(v), "r"(cluster_bar)
-               : "memory");
-}
 
 __device__ __forceinline__ void st_async_v2(uint32_t cluster_addr, uint32_t a, uint32_t b,
                                             uint32_t cluster_bar) {
@@ -234,11 +213,6 @@ __device__ __forceinline__ bool named_bar_red_or(uint32_t id, uint32_t nthreads,
   return r != 0;
 }
 
-// ---------------------------------------------------------------- tcgen05
-// Tensor-memory address: bits 31..16 lane, bits 15..0 column (32-bit cells).
-__device__ __forceinline__ uint32_t tmem_addr(uint32_t base, uint32_t lane, uint32_t col) {
-  return base + (lane << 16) + col;
-}
 
 __device__ __forceinline__ void tmem_alloc(uint32_t dst_smem, uint32_t ncols) {
   asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem),
@@ -260,44 +234,18 @@ __device__ __forceinline__ void tc_fence_after() {
   asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 }
 
-// D[tmem] (+)= A[smem desc] * B[smem desc], kind::f16 (bf16 in, fp32 acc).
-__device__ __forceinline__ void mma_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
-                                       uint32_t idesc, uint32_t accumulate) {
-  asm volatile(
-      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
-      " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}" ::"r"(d_tmem),
-      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
 
-// D[tmem] (+)= A[tmem] * B[smem desc], kind::f16.
-__device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
-                                       uint32_t idesc, uint32_t accumulate) {
-  asm volatile(
-      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
-      " tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}" ::"r"(d_tmem),
-      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
-
-// The same two MMA forms issued by one elected lane of a converged warp (the
-// whole warp executes the call; elect.sync picks the lowest active lane).
-// Issuing from a converged warp keeps the issue cost negligible.
+// ---------------------------------------------------------------- tcgen05.mma
+// D (tensor memory, fp32) [+]= A * B, kind::f16 (bf16 operands), issued by one
+// elected lane of a converged warp (the whole warp executes the call;
+// elect.sync picks the lowest active lane), which keeps the issue cost
+// negligible.  A and B from shared memory (matrix descriptors).
 __device__ __forceinline__ void mma_ss_elect(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
                                              uint32_t idesc, uint32_t accumulate) {
   asm volatile(
       "{\n .reg .pred e, p;\n elect.sync _|e, 0xffffffff;\n setp.ne.b32 p, %4, 0;\n"
       " @e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}" ::"r"(d_tmem),
       "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
-
-__device__ __forceinline__ void mma_ts_elect(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
-                                             uint32_t idesc, uint32_t accumulate) {
-  asm volatile(
-      "{\n .reg .pred e, p;\n elect.sync _|e, 0xffffffff;\n setp.ne.b32 p, %4, 0;\n"
-      " @e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}" ::"r"(d_tmem),
-      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
       : "memory");
 }
 
@@ -338,22 +286,7 @@ __device__ __forceinline__ void mma_commit_mc_elect(uint32_t bar, uint16_t mask)
       : "memory");
 }
 
-// Arrive once on `bar` when all previously issued tcgen05 ops of this thread
-// have completed.
-__device__ __forceinline__ void mma_commit(uint32_t bar) {
-  asm volatile(
-      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
-      : "memory");
-}
 
-// Same, arriving on the barrier at the same offset in every CTA of `mask`.
-__device__ __forceinline__ void mma_commit_mc(uint32_t bar, uint16_t mask) {
-  asm volatile(
-      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
-      " [%0], %1;" ::"r"(bar),
-      "h"(mask)
-      : "memory");
-}
 
 // Instruction descriptor, kind::f16: fp32 accumulator, bf16 A and B,
 // M = 128, N given; a/b major: 0 = K-major, 1 = MN-major.

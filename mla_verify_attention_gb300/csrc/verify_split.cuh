@@ -19,20 +19,24 @@
 //
 //   S CTA (cluster rank 0): Q[128 x 576] bf16 lives in tensor memory and is
 //     the A operand of S = Q K^T (tcgen05.mma, M=128, N=64 keys, K=576, fp32
-//     accumulator in tensor memory, double-buffered).  Four softmax warps own
-//     one row each per thread: scale, tree mask, running max with lazy
-//     rescaling, exp2, running sum, and bf16 P.  P (plus per-row rescale
-//     factors) is pushed into the O CTA's shared memory with st.async.
+//     scores in tensor memory, double-buffered).  Eight softmax warps, two
+//     threads per row (32 keys each): scale, tree mask, running max with lazy
+//     rescaling, exp2, running sum, and bf16 P, staged in shared memory with
+//     the per-row rescale factors and moved into the O CTA by one bulk copy
+//     per tile.
 //   O CTA (cluster rank 1): owns the 128 x 512 fp32 accumulator, i.e. all 512
 //     tensor-memory columns.  Its MMA warp runs O += P V with P (K-major) and
 //     V (MN-major, the latent part of the same cache rows) from shared memory,
-//     N=256 per instruction.  Four warps rescale O rows when the S CTA raised
-//     a row's max, zero cache rows past the stream end, and write the result.
+//     N=256 per instruction.  Eight helper warps rescale O rows when the S CTA
+//     raised a row's max, zero cache rows past the slice end, and write the
+//     result through shared memory and TMA tensor stores.
 //
-// Each CTA streams the cache slice it needs straight from HBM/L2 with TMA
-// (128-byte swizzle).  P is rounded to bf16 because V is bf16 in the cache;
-// for short streams (where a few keys carry most of the weight) P is sent as
-// two bf16 terms hi + lo and the PV product is issued once per term.
+// Each CTA streams the cache slice it needs with TMA (128-byte swizzle), from
+// a contiguous cache or from pages of a multiple of 64 keys; for other page
+// sizes a second instantiation of the kernel gathers rows with cp.async into
+// the same layout.  P is rounded to bf16 because V is bf16 in the cache; for
+// short streams (where a few keys carry most of the weight) P is sent as two
+// bf16 terms hi + lo and the PV product is issued once per term.
 #pragma once
 #include <cstdint>
 #include <cstdio>
