@@ -230,6 +230,18 @@ def run_reference(args, rank):
     print(json.dumps(line), flush=True)
 
 
+def max_over_ranks(value, world, device=None):
+    """The largest of the ranks' values, returned on every rank (replicas run in
+    lock step, so the job's time per call is its slowest rank's)."""
+    if world <= 1:
+        return value
+    import torch
+    import torch.distributed as tdist
+    v = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    tdist.all_reduce(v, op=tdist.ReduceOp.MAX)
+    return float(v.item())
+
+
 def case_seed_for_pages(case):
     """Seed of the page order of a bench case (fixed per workload shape)."""
     return 0x5041 + int(case.Smax)
@@ -329,11 +341,7 @@ def run_ours(args, rank, world, local_rank):
         tdist.barrier()
     clocks = sampler.stop(window=(t_wall0, t_wall1))
     ms = ev0.elapsed_time(ev1)
-    us_call = ms * 1e3 / args.steps
-    if dist:
-        v = torch.tensor([us_call], device=dev)
-        tdist.all_reduce(v, op=tdist.ReduceOp.MAX)
-        us_call = float(v.item())
+    us_call = max_over_ranks(ms * 1e3 / args.steps, world, dev)
     st = mva.last_device_error()
     if st != 0:
         raise mva.MLAError(st, "timed region")
