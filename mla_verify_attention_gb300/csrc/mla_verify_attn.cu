@@ -21,7 +21,10 @@ namespace {
 __device__ unsigned int g_mla_status;
 
 constexpr int kMaxDevices = 64;
-constexpr int kMinTilesPerSlice = 8;          // shortest slice worth a cluster's start-up
+// Shortest slice: a slice of a short stream still pays the unit's fixed cost
+// (Q load, epilogue) and adds a partial to merge.  Measured on tree9/chain9
+// shapes: 2-tile slices beat longer ones while all units fit one wave.
+constexpr int kMinTilesPerSlice = 2;
 constexpr int kTwoTermMaxKeys = 4096;         // streams up to this length send P as hi + lo
 constexpr size_t kSmemBytes = sizeof(mla::Smem) + 1024;   // + manual 1 KB alignment
 

@@ -74,11 +74,13 @@ def test_plan_arithmetic(lib):
     assert mva.plan(1, 9, 64, 65600, 76) == (5, 15, 69)
     # 33 drafts over 16k: 17 row tiles, 4 slices.
     assert mva.plan(1, 33, 64, 16448, 76) == (17, 4, 65)
-    # short prefix: slices shorter than 8 tiles are not worth a cluster
-    assert mva.plan(1, 9, 64, 320, 76) == (5, 1, 5)
+    # short prefix: slices are at least 2 tiles long
+    assert mva.plan(1, 9, 64, 320, 76) == (5, 3, 2)
+    # 4k prefix: 15 slices would be wanted; 5-tile slices give 13
+    assert mva.plan(1, 9, 64, 4160, 76) == (5, 13, 5)
     # ragged batch: smaller slices for balance
     nrt, ns, ct = mva.plan(8, 9, 64, 32832, 76)
-    assert nrt == 5 and ns * ct >= 513 and (ns - 1) * ct < 513 and ct >= 8
+    assert nrt == 5 and ns * ct >= 513 and (ns - 1) * ct < 513 and ct >= 2
     # H other than 64 and one query row
     assert mva.plan(1, 1, 1, 64, 76)[0] == 1
     assert mva.plan(2, 3, 16, 1000, 76)[0] == 1
