@@ -142,6 +142,11 @@ int mla_verify_attn_paged(const void* q_nope_abs, const void* q_rope, const void
  * word: MLA_OK, MLA_ERR_SEQLEN, MLA_ERR_DEVICE_TIMEOUT or MLA_ERR_PAGE (the first recorded),
  * or MLA_ERR_LAUNCH if the synchronisation itself failed.  The word is shared
  * by all calls on the device since it was last read.
+ * Every internal pipeline wait gives up after 2 s; the call's kernels then
+ * unwind (waiting, again bounded, for their own copies in flight) and leave
+ * the context usable.  For testing that path, a non-empty environment
+ * variable MLA_VERIFY_TEST_STALL other than "0" makes one work unit of each
+ * later call withhold one of its cache loads.
  */
 int mla_verify_attn_last_device_error(cudaStream_t stream);
 

@@ -320,6 +320,8 @@ int run(const Call& c) {
   p.nsplit = ns;
   p.chunk_tiles = ct;
   p.two_term_max_keys = kTwoTermMaxKeys;
+  const char* stall = std::getenv("MLA_VERIFY_TEST_STALL");
+  p.test_stall = (stall && stall[0] && stall[0] != '0') ? 1 : 0;
   p.scale_log2 = scale * 1.4426950408889634f;
   p.block_table = c.block_table;
   p.max_blocks = paged ? c.max_blocks : 0;

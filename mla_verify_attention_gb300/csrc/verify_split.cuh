@@ -106,6 +106,9 @@ struct SplitParams {
   const int32_t* block_table;   // [B][max_blocks]
   int max_blocks, page_size, pool_pages;
   const uint8_t* kv_pool;       // gather kernel: the pool's first row
+  // Test hook (MLA_VERIFY_TEST_STALL): unit 0 never loads the second part of
+  // key tile 0, so its bounded waits run out and report MLA_ERR_DEVICE_TIMEOUT.
+  int test_stall;
 };
 
 // Gather mode: warps 0, 2 and 3 of each CTA copy cache rows (16 bytes per copy).
@@ -298,6 +301,7 @@ __device__ __forceinline__ void s_producer(Smem& sm, const Unit& u, const SplitP
     const int slot = j % kKSlots;
 #pragma unroll
     for (int part = 0; part < 2; ++part) {
+      if (p.test_stall && blockIdx.x == 0 && j == 0 && part == 1) continue;
       if (!wait_or_abort(sm, smem_u32(&sm.kempty[part][slot]), ((j / kKSlots) & 1) ^ 1, p, 2))
         return;
       const uint32_t full = smem_u32(&sm.kfull[part][slot]);
