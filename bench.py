@@ -292,10 +292,16 @@ def run_ours(args, rank, world, local_rank):
         Smax = table.shape[1] * args.page_size      # the paged call's key bound
     out = torch.empty((B, q, H, 512), dtype=torch.float32, device=dev)
     lse = torch.empty((B, q, H), dtype=torch.float32, device=dev)
-    need = mva.workspace_size(B, q, H, Smax)
+    if paged:
+        need = mva.paged_workspace_size(B, q, H, table.shape[1], args.page_size)
+    else:
+        need = mva.workspace_size(B, q, H, Smax)
     ws = torch.empty(max(need, 1), dtype=torch.uint8, device=dev)
     n_rt, nsplit, chunk = mva.plan(B, q, H, Smax)
-    launches_per_call = 1 + (1 if nsplit > 1 else 0)
+    # split kernel, the slice merge when the keys are split, and for pages
+    # that are not whole 64-key tiles the copy into a contiguous cache
+    copied = paged and args.page_size % 64 != 0
+    launches_per_call = 1 + (1 if nsplit > 1 else 0) + (1 if copied else 0)
     stream = torch.cuda.current_stream(dev)
     sh = int(stream.cuda_stream)
     ptrs = [q_nope.data_ptr(), q_rope.data_ptr(), None, seq.data_ptr(), mask.data_ptr()]
@@ -420,7 +426,7 @@ def run_ours(args, rank, world, local_rank):
     roof["traffic"] = recorded_traffic(args.workload)
     roof["peak_source"] = "%s (MEASURED_PEAKS.json burst)" % peak_src if peak_src == "measured" \
         else "fallback"
-    roof["kernel"] = "verify_split_kernel (launch 1 of %d per call)" % launches_per_call
+    roof["kernel"] = "verify_split_kernel (%d launches per call)" % launches_per_call
     roof["kernel_us"] = split_us
     roof["call_us"] = us_call
     roof["call_frac"] = (flops / (us_call * 1e-6) / 1e12) / bf16_tf if t_tensor >= t_hbm else \

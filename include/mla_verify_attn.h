@@ -110,8 +110,11 @@ int mla_verify_attn(const void* q_nope_abs, const void* q_rope, const void* kv,
  * name a paged cache (page_size 1, scattered rows) as the production layout
  * (page "The Moment of Truth: Benchmarking a Custom sm_120 Flash Attention
  * Kernel", section "Output Knowledge Created").  Pages of a multiple of 64 keys
- * keep whole-tile TMA loads; any other page size (1 included) gathers rows
- * with 16-byte cp.async copies.  The computation is that of mla_verify_attn with
+ * are read in place with whole-tile TMA loads; for any other page size (1
+ * included) a first kernel copies each stream's rows, in key order, into a
+ * contiguous cache in the workspace, which the split kernel then reads (the
+ * results equal the contiguous call's bit for bit).  The computation is that
+ * of mla_verify_attn with
  *   kv[b, t, :] = kv_pool[block_table[b, t / page_size] * page_size + t % page_size, :]
  * i.e. key t of stream b lives in page block_table[b][t / page_size] of the pool.
  *
@@ -125,12 +128,23 @@ int mla_verify_attn(const void* q_nope_abs, const void* q_rope, const void* kv,
  *                reported as MLA_ERR_PAGE through the device status (that
  *                stream's results are then undefined).
  *   max_blocks   blocks per stream in block_table; Smax = max_blocks * page_size
- *                (< 2^24) bounds seq_lens[b] and sizes the workspace
- *                (mla_verify_attn_workspace_size(B, q_len, H, Smax)).
+ *                (< 2^24) bounds seq_lens[b].
+ *   workspace    at least mla_verify_attn_paged_workspace_size(B, q_len, H,
+ *                max_blocks, page_size) bytes (MLA_ERR_WORKSPACE otherwise).
  *   page_size    keys per page, >= 1 (MLA_ERR_SHAPE otherwise).  Multiples of 64
  *                are the fast path: a 64-key tile then never crosses a page.
  * All other arguments, results and errors as for mla_verify_attn.
  */
+/*
+ * Workspace bytes mla_verify_attn_paged needs on the current device: that of
+ * mla_verify_attn for Smax = max_blocks * page_size, plus, when page_size is
+ * not a multiple of 64, a contiguous copy of the cache (B * Smax * 1152 bytes,
+ * after the partials at a 256-byte boundary).  0 for arguments the call would
+ * reject (and, like mla_verify_attn_workspace_size, without a usable device).
+ * Host-only.
+ */
+size_t mla_verify_attn_paged_workspace_size(int B, int q_len, int H, int max_blocks, int page_size);
+
 int mla_verify_attn_paged(const void* q_nope_abs, const void* q_rope, const void* kv_pool,
                           long long pool_rows, const int32_t* block_table, int max_blocks,
                           int page_size, const int32_t* seq_lens, const uint32_t* tree_mask, int B,

@@ -19,7 +19,9 @@ STATUS_NAMES = {
     -7: "MLA_ERR_DEVICE_TIMEOUT", -8: "MLA_ERR_SEQLEN", -9: "MLA_ERR_ARG", -10: "MLA_ERR_PAGE",
 }
 EXPORTED = ("mla_verify_attn", "mla_verify_attn_workspace_size", "mla_verify_attn_last_device_error",
-            "mla_verify_attn_strerror", "mla_verify_attn_plan")
+            "mla_verify_attn_strerror", "mla_verify_attn_plan", "mla_verify_attn_paged",
+            "mla_verify_attn_paged_workspace_size", "mla_verify_attn_set_timing_events",
+            "mla_verify_attn_noalloc")
 
 _lock = threading.Lock()
 _lib = None
@@ -54,6 +56,8 @@ def load_library(build_if_missing: bool = True) -> ctypes.CDLL:
         L = ctypes.c_longlong
         lib.mla_verify_attn_paged.argtypes = [P, P, P, L, P, I, I, P, P, I, I, I, F, P, P, P, Z, P]
         lib.mla_verify_attn_paged.restype = I
+        lib.mla_verify_attn_paged_workspace_size.argtypes = [I, I, I, I, I]
+        lib.mla_verify_attn_paged_workspace_size.restype = Z
         lib.mla_verify_attn_set_timing_events.argtypes = [P, P]
         lib.mla_verify_attn_set_timing_events.restype = I
         _lib = lib
@@ -79,6 +83,10 @@ def plan(B: int, q_len: int, H: int, Smax: int, max_clusters: int = 0):
 
 def workspace_size(B: int, q_len: int, H: int, Smax: int) -> int:
     return int(load_library().mla_verify_attn_workspace_size(B, q_len, H, Smax))
+
+
+def paged_workspace_size(B: int, q_len: int, H: int, max_blocks: int, page_size: int) -> int:
+    return int(load_library().mla_verify_attn_paged_workspace_size(B, q_len, H, max_blocks, page_size))
 
 
 def _stream_handle(stream) -> int:
@@ -140,7 +148,9 @@ def verify_attn_paged(q_nope, q_rope, kv_pool, block_table, page_size, seq_lens,
 
     kv_pool [pool_rows, 576] bf16 (pages of page_size rows), block_table
     [B, max_blocks] int32 (page of each page_size-key block of each stream),
-    page_size a positive multiple of 64; other arguments as for verify_attn.
+    page_size >= 1 (multiples of 64 are read in place; other sizes are first
+    copied into a contiguous cache in the workspace); other arguments as for
+    verify_attn.
     """
     import torch
     B, q, H, Dl = q_nope.shape
@@ -162,7 +172,7 @@ def verify_attn_paged(q_nope, q_rope, kv_pool, block_table, page_size, seq_lens,
         out = torch.empty((B, q, H, 512), dtype=torch.float32, device=dev)
     if lse is None:
         lse = torch.empty((B, q, H), dtype=torch.float32, device=dev)
-    need = workspace_size(B, q, H, max_blocks * page_size)
+    need = paged_workspace_size(B, q, H, max_blocks, int(page_size))
     if workspace is None and need > 0:
         workspace = torch.empty(need, dtype=torch.uint8, device=dev)
     ws_ptr = workspace.data_ptr() if workspace is not None else 0

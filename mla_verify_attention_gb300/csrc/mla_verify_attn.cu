@@ -13,6 +13,7 @@
 #include "mla_verify_attn.h"
 #include "combine.cuh"
 #include "verify_split.cuh"
+#include "repack.cuh"
 
 namespace {
 
@@ -147,6 +148,17 @@ size_t workspace_bytes_for(int B, int q, int H, int nsplit) {
 
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
 
+// A paged call whose pages are not whole 64-key tiles keeps, after the split
+// partials in its workspace (at a 256-byte boundary), a contiguous copy of the
+// cache: [B][Smax][576] bf16.
+bool needs_copy(int page_size) { return page_size % mla::kKeys != 0; }
+size_t copy_offset(size_t partial_bytes) { return (partial_bytes + 255) & ~static_cast<size_t>(255); }
+size_t copy_bytes(int B, int Smax) { return static_cast<size_t>(B) * Smax * (576 * 2); }
+bool paged_args_ok(int max_blocks, int page_size) {
+  return page_size >= 1 && max_blocks >= 1 &&
+         static_cast<long long>(max_blocks) * page_size < (1LL << 24);
+}
+
 int encode(DeviceInfo* d, CUtensorMap* map, const void* base, int rank, const cuuint64_t* dims,
            const cuuint64_t* strides, const cuuint32_t* box,
            CUtensorMapDataType dtype = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16) {
@@ -201,6 +213,15 @@ size_t mla_verify_attn_workspace_size(int B, int q_len, int H, int Smax) {
   return workspace_bytes_for(B, q_len, H, ns);
 }
 
+size_t mla_verify_attn_paged_workspace_size(int B, int q_len, int H, int max_blocks, int page_size) {
+  if (!paged_args_ok(max_blocks, page_size)) return 0;
+  const int Smax = max_blocks * page_size;
+  const size_t partials = mla_verify_attn_workspace_size(B, q_len, H, Smax);
+  if (!needs_copy(page_size)) return partials;
+  if (!shape_ok(B, q_len, H, Smax)) return 0;
+  return copy_offset(partials) + copy_bytes(B, Smax);
+}
+
 }  // extern "C"
 
 namespace {
@@ -227,7 +248,6 @@ struct Call {
 int run(const Call& c) {
   const void* q_nope_abs = c.q_nope_abs;
   const void* q_rope = c.q_rope;
-  const void* kv = c.kv;
   const int32_t* seq_lens = c.seq_lens;
   const uint32_t* tree_mask = c.tree_mask;
   const int B = c.B, q_len = c.q_len, H = c.H, Smax = c.Smax;
@@ -237,13 +257,16 @@ int run(const Call& c) {
   void* workspace = c.workspace;
   const size_t workspace_bytes = c.workspace_bytes;
   cudaStream_t stream = c.stream;
-  const bool paged = c.block_table != nullptr;
+  // Paged caches: pages of a multiple of 64 keys are read in place (TMA tiles
+  // through the block table); others are first copied into the workspace.
+  const bool copy = c.block_table != nullptr && needs_copy(c.page_size);
+  const bool paged = c.block_table != nullptr && !copy;
   if (!shape_ok(B, q_len, H, Smax)) return MLA_ERR_SHAPE;
   if (!std::isfinite(scale)) return MLA_ERR_ARG;
   if (B == 0) return MLA_OK;
-  if (!q_nope_abs || !q_rope || !kv || !seq_lens || !tree_mask || !out || !lse)
+  if (!q_nope_abs || !q_rope || !c.kv || !seq_lens || !tree_mask || !out || !lse)
     return MLA_ERR_NULLPTR;
-  if (!aligned(q_nope_abs, 16) || !aligned(q_rope, 16) || !aligned(kv, 16) || !aligned(out, 16) ||
+  if (!aligned(q_nope_abs, 16) || !aligned(q_rope, 16) || !aligned(c.kv, 16) || !aligned(out, 16) ||
       !aligned(lse, 4) || !aligned(seq_lens, 4) || !aligned(tree_mask, 4) ||
       (workspace && !aligned(workspace, 256)))
     return MLA_ERR_ALIGN;
@@ -254,8 +277,12 @@ int run(const Call& c) {
   int nrt, ns, ct;
   st = plan(B, q_len, H, Smax, d->max_clusters, &nrt, &ns, &ct);
   if (st != MLA_OK) return st;
-  const size_t need = workspace_bytes_for(B, q_len, H, ns);
+  const size_t partials = workspace_bytes_for(B, q_len, H, ns);
+  const size_t need = copy ? copy_offset(partials) + copy_bytes(B, Smax) : partials;
   if (need > 0 && (!workspace || workspace_bytes < need)) return MLA_ERR_WORKSPACE;
+  // The cache the split kernel reads: the caller's, or the contiguous copy.
+  const void* kv = copy ? static_cast<const void*>(static_cast<char*>(workspace) + copy_offset(partials))
+                        : c.kv;
 
   const long long rows = static_cast<long long>(B) * q_len * H;
   // Tensor maps.  Each cache (and q_nope) row of 576 (512) bf16 is viewed as
@@ -323,28 +350,53 @@ int run(const Call& c) {
   const char* stall = std::getenv("MLA_VERIFY_TEST_STALL");
   p.test_stall = (stall && stall[0] && stall[0] != '0') ? 1 : 0;
   p.scale_log2 = scale * 1.4426950408889634f;
-  p.block_table = c.block_table;
+  p.block_table = paged ? c.block_table : nullptr;
   p.max_blocks = paged ? c.max_blocks : 0;
   p.page_size = paged ? c.page_size : 0;
   p.pool_pages = paged ? static_cast<int>(c.pool_rows / c.page_size) : 0;
-  // Pages that are not whole 64-key tiles: the kernel that gathers rows with cp.async.
-  const bool gather = paged && c.page_size % mla::kKeys != 0;
-  p.kv_pool = static_cast<const uint8_t*>(kv);
-
   const long long units = static_cast<long long>(B) * nrt * ns;
   if (2 * units >= (1LL << 31)) return MLA_ERR_SHAPE;
+  if (copy) {
+    mla::RepackParams rp;
+    rp.pool = static_cast<const uint8_t*>(c.kv);
+    rp.block_table = c.block_table;
+    rp.seq_lens = seq_lens;
+    rp.dst = static_cast<uint8_t*>(const_cast<void*>(kv));
+    rp.status = d->status_word;
+    rp.B = B;
+    rp.max_blocks = c.max_blocks;
+    rp.page_size = c.page_size;
+    rp.pool_pages = static_cast<int>(c.pool_rows / c.page_size);
+    rp.Smax = Smax;
+    const dim3 grid((Smax + mla::kKeys - 1) / mla::kKeys, B < 65535 ? B : 65535, 1);
+    mla::repack_kernel<<<grid, mla::kRepackThreads, 0, stream>>>(rp);
+    if (cudaGetLastError() != cudaSuccess) return MLA_ERR_LAUNCH;
+  }
   const bool timing = g_timing_before != nullptr;
+  // After the cache copy the split kernel is its programmatic dependent
+  // (prologue overlapped, cache loads wait for the copy to complete).
+  const bool after_copy = copy && !timing;
   if (timing && cudaEventRecord(g_timing_before, stream) != cudaSuccess) {
     cudaGetLastError();
     return MLA_ERR_LAUNCH;
   }
-  if (gather)
-    mla::verify_split_kernel<true><<<static_cast<unsigned>(2 * units), mla::kThreads, kSmemBytes,
-                                     stream>>>(map_qn, map_qr, map_kvs0, map_kvs1, map_kvo, map_out, p);
-  else
-    mla::verify_split_kernel<false><<<static_cast<unsigned>(2 * units), mla::kThreads, kSmemBytes,
-                                      stream>>>(map_qn, map_qr, map_kvs0, map_kvs1, map_kvo, map_out, p);
-  if (cudaGetLastError() != cudaSuccess) return MLA_ERR_LAUNCH;
+  {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(2 * units), 1, 1);
+    cfg.blockDim = dim3(mla::kThreads, 1, 1);
+    cfg.dynamicSmemBytes = kSmemBytes;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = after_copy ? 1 : 0;
+    if (cudaLaunchKernelEx(&cfg, after_copy ? mla::verify_split_kernel<true> : mla::verify_split_kernel<false>,
+                           map_qn, map_qr, map_kvs0, map_kvs1, map_kvo, map_out, p) != cudaSuccess) {
+      cudaGetLastError();
+      return MLA_ERR_LAUNCH;
+    }
+  }
   if (timing && cudaEventRecord(g_timing_after, stream) != cudaSuccess) {
     cudaGetLastError();
     return MLA_ERR_LAUNCH;
@@ -400,9 +452,8 @@ int mla_verify_attn_paged(const void* q_nope_abs, const void* q_rope, const void
                           int page_size, const int32_t* seq_lens, const uint32_t* tree_mask, int B,
                           int q_len, int H, float scale, float* out, float* lse, void* workspace,
                           size_t workspace_bytes, cudaStream_t stream) {
-  if (page_size < 1 || max_blocks < 1 || pool_rows < 1 ||
-      pool_rows % page_size != 0 || pool_rows >= (1LL << 31) ||
-      static_cast<long long>(max_blocks) * page_size >= (1LL << 24))
+  if (!paged_args_ok(max_blocks, page_size) || pool_rows < 1 || pool_rows % page_size != 0 ||
+      pool_rows >= (1LL << 31))
     return MLA_ERR_SHAPE;
   if (B > 0 && (!block_table || !kv_pool)) return MLA_ERR_NULLPTR;
   if (block_table && !aligned(block_table, 4)) return MLA_ERR_ALIGN;

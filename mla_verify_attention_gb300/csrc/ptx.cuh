@@ -94,6 +94,17 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint64_
   }
 }
 
+// ---------------------------------------------------------------- grid dependencies
+// Block until the grids this one depends on programmatically have completed
+// and their memory is visible (a no-op for a launch without that dependency).
+__device__ __forceinline__ void grid_dependency_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+// Let the dependent grid be scheduled once every CTA of this grid got here.
+__device__ __forceinline__ void grid_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ---------------------------------------------------------------- proxies
 __device__ __forceinline__ void fence_proxy_async() {
   asm volatile("fence.proxy.async;" ::: "memory");
@@ -162,23 +173,6 @@ template <int N>
 __device__ __forceinline__ void bulk_wait_read() {
   asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
 }
-// 16-byte asynchronous copy global -> shared, cached in L2 only.  No memory
-// clobber, so the compiler may batch the loads that compute the addresses of
-// consecutive copies; callers never read a destination before the copy is
-// complete, and the copies keep their order relative to the other volatile
-// cp.async statements (arrive, wait), which do clobber memory.
-__device__ __forceinline__ void cp_async_16(uint32_t dst, const void* src) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src));
-}
-// One arrival on `bar` once all of this thread's earlier cp.async copies have
-// completed; the barrier's expected count already includes it (noinc).
-__device__ __forceinline__ void cp_async_arrive_noinc(uint32_t bar) {
-  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
-}
-__device__ __forceinline__ void cp_async_wait_all() {
-  asm volatile("cp.async.wait_all;" ::: "memory");
-}
-
 // Wait until every committed bulk group has completed (its writes performed).
 __device__ __forceinline__ void bulk_wait_all() {
   asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");

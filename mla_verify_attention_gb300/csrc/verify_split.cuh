@@ -32,9 +32,8 @@
 //     result through shared memory and TMA tensor stores.
 //
 // Each CTA streams the cache slice it needs with TMA (128-byte swizzle), from
-// a contiguous cache or from pages of a multiple of 64 keys; for other page
-// sizes a second instantiation of the kernel gathers rows with cp.async into
-// the same layout.  P is rounded to bf16 because V is bf16 in the cache; for
+// a contiguous cache or from pages of a multiple of 64 keys (caches with other
+// page sizes are first copied into a contiguous one, see repack.cuh).  P is rounded to bf16 because V is bf16 in the cache; for
 // short streams (where a few keys carry most of the weight) P is sent as two
 // bf16 terms hi + lo and the PV product is issued once per term.
 #pragma once
@@ -101,19 +100,13 @@ struct SplitParams {
   float scale_log2;   // scale * log2(e)
   // Paged cache (null block_table: contiguous [B][Smax][576] cache).  Key k of
   // stream b is row block_table[b][k / page_size] * page_size + k % page_size of
-  // the page pool.  Pages of a multiple of 64 keys keep the TMA tile loads
-  // (no tile crosses a page); other page sizes gather rows with cp.async.
+  // the page pool, with page_size a multiple of 64 (no tile crosses a page).
   const int32_t* block_table;   // [B][max_blocks]
   int max_blocks, page_size, pool_pages;
-  const uint8_t* kv_pool;       // gather kernel: the pool's first row
   // Test hook (MLA_VERIFY_TEST_STALL): unit 0 never loads the second part of
   // key tile 0, so its bounded waits run out and report MLA_ERR_DEVICE_TIMEOUT.
   int test_stall;
 };
-
-// Gather mode: warps 0, 2 and 3 of each CTA copy cache rows (16 bytes per copy).
-constexpr int kGatherThreads = 96;
-constexpr uint32_t kGatherBar = 5;               // named barrier of the gather threads
 
 struct __align__(1024) Smem {
   uint8_t ring[kRingBytes];
@@ -127,7 +120,6 @@ struct __align__(1024) Smem {
   uint64_t vfull[kVSlots], vempty[kVSlots];
   uint64_t pfull[2];
   uint64_t odone, corrgo, corrdone, mlfull, drain;
-  int32_t grow[2][kKeys];    // gather mode: pool rows of a tile's keys (two tiles in flight)
   uint32_t tmem_base;
   uint32_t abort_flag;
   uint32_t cmd;
@@ -169,9 +161,9 @@ __device__ __forceinline__ Unit decode_unit(const SplitParams& p) {
 // TMA coordinates (row, stream) of the first key of a 64-key tile: the key
 // within stream b of the contiguous cache, or the row of the page pool.  A
 // block-table entry outside the pool is reported and replaced by page 0.
-// (Cache layout and gather mode are template parameters of the producer and
-// MMA roles: a per-tile runtime test in the MMA warps' loops measurably slowed
-// the MMA issue even when never taken.)
+// (The cache layout is a template parameter of the producers: a per-tile
+// runtime test in the MMA warps' loops had measurably slowed the MMA issue
+// even when never taken.)
 template <bool kPaged>
 __device__ __forceinline__ int2 tile_origin(const SplitParams& p, const Unit& u, int key) {
   if (!kPaged) return make_int2(key, u.b);
@@ -182,47 +174,6 @@ __device__ __forceinline__ int2 tile_origin(const SplitParams& p, const Unit& u,
     page = 0;
   }
   return make_int2(page * p.page_size + (key - blk * p.page_size), 0);
-}
-
-// Gather mode: pool row of cache key `key` of stream b (keys below the stream
-// length only).  Entries outside the pool are reported and replaced by page 0.
-__device__ __forceinline__ int32_t gather_row(const SplitParams& p, const Unit& u, int key) {
-  const int blk = key / p.page_size;
-  int page = __ldg(p.block_table + static_cast<size_t>(u.b) * p.max_blocks + blk);
-  if (page < 0 || page >= p.pool_pages) {
-    atomicOr(p.status, kStatusPage);
-    page = 0;
-  }
-  return page * p.page_size + (key - blk * p.page_size);
-}
-
-// Gather mode: copy chunks [c0, c0 + NC) of a tile's keys (rows[k] >= 0) into a
-// tile buffer in the layout TMA produces: [chunk][key][64 dims], 128-byte
-// swizzled.  g = 0 .. kGatherThreads-1; consecutive threads copy consecutive
-// 16-byte pieces of one row.
-template <int NC>
-__device__ __forceinline__ void gather_tile(const SplitParams& p, const int32_t* rows, uint32_t tile,
-                                            int c0, int g) {
-  constexpr int kPerKey = NC * 8;
-#pragma unroll 4
-  for (int i = g; i < kKeys * kPerKey; i += kGatherThreads) {
-    const int k = i / kPerKey;
-    const int rem = i - k * kPerKey;
-    const int c = c0 + (rem >> 3);
-    const int unit = rem & 7;
-    const int32_t row = rows[k];
-    if (row < 0) continue;
-    cp_async_16(tile + c * kChunk + k * 128 + ((unit ^ (k & 7)) << 4),
-                p.kv_pool + static_cast<size_t>(row) * ((kDl + kDr) * 2) + c * 128 + unit * 16);
-  }
-}
-
-// Gather mode: pool row of key k of tile j (-1 past the slice), looked up by
-// thread g = k one tile ahead of its use.
-__device__ __forceinline__ int32_t gather_lookup(const SplitParams& p, const Unit& u, int j, int g) {
-  if (g >= kKeys || j >= u.ntiles) return -1;
-  const int key = u.k0 + j * kKeys + g;
-  return key < u.k1 ? gather_row(p, u, key) : -1;
 }
 
 // Bounded wait that also gives up as soon as another warp of the CTA aborted.
@@ -271,7 +222,7 @@ __device__ __forceinline__ void drain_ring(const uint64_t* full, int nslots, int
 
 // ============================================================ S CTA roles
 
-template <bool kPaged>
+template <bool kPaged, bool kAfterCopy>
 __device__ __forceinline__ void s_producer(Smem& sm, const Unit& u, const SplitParams& p,
                                            const CUtensorMap* map_qn, const CUtensorMap* map_qr,
                                            const CUtensorMap* map_kv0, const CUtensorMap* map_kv1,
@@ -287,6 +238,7 @@ __device__ __forceinline__ void s_producer(Smem& sm, const Unit& u, const SplitP
   // The Q staging area overlaps the first ring slots: wait until the softmax
   // warps have moved Q into tensor memory.
   if (!wait_or_abort(sm, smem_u32(&sm.qready), 0, p, 1)) return;
+  if (kAfterCopy) grid_dependency_wait();   // the cache is the preceding grid's copy
   fence_proxy_async();
   // Two boxes per 64-key tile: [5 chunks][64 keys][64 dims] and [4 chunks][64][64].
   // A part's buffer is refilled as soon as the MMAs that read it are done, so
@@ -313,49 +265,8 @@ __device__ __forceinline__ void s_producer(Smem& sm, const Unit& u, const SplitP
   }
 }
 
-// Gather-mode S producer (kGatherThreads threads, index g): Q by TMA (g = 0),
-// key tiles row by row with cp.async, one arrival per thread and part.
-__device__ __forceinline__ void s_gather_producer(Smem& sm, const Unit& u, const SplitParams& p,
-                                                  const CUtensorMap* map_qn,
-                                                  const CUtensorMap* map_qr, int g) {
-  const uint32_t ring = smem_u32(sm.ring);
-  if (g == 0) {
-    const uint32_t qfull = smem_u32(&sm.qfull);
-    const int y = u.b * u.rows_total + u.row0;
-    mbar_arrive_expect_tx(qfull, kKChunks * kQChunk);
-    tma_load_3d(ring, map_qn, 0, y, 0, qfull);
-    tma_load_2d(ring + kVChunks * kQChunk, map_qr, 0, y, qfull);
-  }
-  // Rows of tile j are looked up during tile j-1 and published through
-  // sm.grow[j & 1]; the barrier of tile j+1 is passed only after every thread
-  // finished reading grow[(j+1) & 1] at tile j-1, so each buffer is free again.
-  int32_t next = gather_lookup(p, u, 0, g);
-  // The Q staging area overlaps the first ring slots.
-  bool ok = wait_or_abort(sm, smem_u32(&sm.qready), 0, p, 1);
-  for (int j = 0; j < u.ntiles; ++j) {
-    if (g < kKeys) sm.grow[j & 1][g] = next;
-    next = gather_lookup(p, u, j + 1, g);
-    if (named_bar_red_or(kGatherBar, kGatherThreads, !ok)) break;
-    const int slot = j % kKSlots;
-    const uint32_t tile = ring + slot * kKTile;
-    ok = wait_or_abort(sm, smem_u32(&sm.kempty[0][slot]), ((j / kKSlots) & 1) ^ 1, p, 2);
-    if (ok) {
-      gather_tile<kKSplit>(p, sm.grow[j & 1], tile, 0, g);
-      cp_async_arrive_noinc(smem_u32(&sm.kfull[0][slot]));
-      ok = wait_or_abort(sm, smem_u32(&sm.kempty[1][slot]), ((j / kKSlots) & 1) ^ 1, p, 2);
-    }
-    if (ok) {
-      gather_tile<kKChunks - kKSplit>(p, sm.grow[j & 1], tile, kKSplit, g);
-      cp_async_arrive_noinc(smem_u32(&sm.kfull[1][slot]));
-    }
-  }
-  cp_async_wait_all();
-  if (g == 0) mbar_wait(smem_u32(&sm.qfull), 0, kWaitNs / 2);
-}
-
 // The MMA warp runs converged; one elected lane issues (issue cost then stays
 // negligible next to the 36 MMAs of a tile).
-template <bool kGather>
 __device__ __forceinline__ void s_mma(Smem& sm, const Unit& u, const SplitParams& p,
                                       uint32_t tmem) {
   const uint32_t ring = smem_u32(sm.ring);
@@ -370,7 +281,6 @@ __device__ __forceinline__ void s_mma(Smem& sm, const Unit& u, const SplitParams
     // Descriptor of chunk c = descriptor of chunk 0 + c * 8 KB (in 16-byte units).
     const uint64_t bdesc0 = sdesc_sw128(ring + slot * kKTile, 16, 1024);
     if (!warp_wait(sm, smem_u32(&sm.kfull[0][slot]), (j / kKSlots) & 1, p, 5)) return;
-    if (kGather) fence_proxy_async_smem();   // rows written by cp.async, read by the MMA
     tc_fence_after();
 #pragma unroll
     for (int c = 0; c < kKSplit; ++c)
@@ -378,7 +288,6 @@ __device__ __forceinline__ void s_mma(Smem& sm, const Unit& u, const SplitParams
                          kIdescQK, c != 0);
     mma_commit_elect(smem_u32(&sm.kempty[0][slot]));
     if (!warp_wait(sm, smem_u32(&sm.kfull[1][slot]), (j / kKSlots) & 1, p, 5)) return;
-    if (kGather) fence_proxy_async_smem();
     tc_fence_after();
 #pragma unroll
     for (int c = kKSplit; c < kKChunks; ++c)
@@ -595,10 +504,11 @@ __device__ __forceinline__ void s_softmax(Smem& sm, const Unit& u, const SplitPa
 
 // ============================================================ O CTA roles
 
-template <bool kPaged>
+template <bool kPaged, bool kAfterCopy>
 __device__ __forceinline__ void o_producer(Smem& sm, const Unit& u, const SplitParams& p,
                                            const CUtensorMap* map_kv, int& n_issued) {
   const uint32_t ring = smem_u32(sm.ring);
+  if (kAfterCopy) grid_dependency_wait();   // the cache is the preceding grid's copy
   int2 org0 = tile_origin<kPaged>(p, u, u.k0);
   int2 org1 = u.ntiles > 1 ? tile_origin<kPaged>(p, u, u.k0 + kKeys) : org0;
   for (int j = 0; j < u.ntiles; ++j) {
@@ -612,26 +522,6 @@ __device__ __forceinline__ void o_producer(Smem& sm, const Unit& u, const SplitP
     tma_load_4d(ring + slot * kVTile, map_kv, 0, org.x, 0, org.y, full);
     n_issued = j + 1;
   }
-}
-
-// Gather-mode O producer: value tiles (chunks 0..7) row by row with cp.async.
-__device__ __forceinline__ void o_gather_producer(Smem& sm, const Unit& u, const SplitParams& p,
-                                                  int g) {
-  const uint32_t ring = smem_u32(sm.ring);
-  int32_t next = gather_lookup(p, u, 0, g);
-  bool ok = true;
-  for (int j = 0; j < u.ntiles; ++j) {
-    if (g < kKeys) sm.grow[j & 1][g] = next;
-    next = gather_lookup(p, u, j + 1, g);
-    if (named_bar_red_or(kGatherBar, kGatherThreads, !ok)) break;
-    const int slot = j & 1;
-    ok = wait_or_abort(sm, smem_u32(&sm.vempty[slot]), ((j >> 1) & 1) ^ 1, p, 9);
-    if (ok) {
-      gather_tile<kVChunks>(p, sm.grow[j & 1], ring + slot * kVTile, 0, g);
-      cp_async_arrive_noinc(smem_u32(&sm.vfull[slot]));
-    }
-  }
-  cp_async_wait_all();
 }
 
 __device__ __forceinline__ uint32_t p_tile_bytes(const Unit& u) {
@@ -652,7 +542,6 @@ __device__ __forceinline__ bool o_command(Smem& sm, uint32_t cmd, int& ncmd, con
   return ok;
 }
 
-template <bool kGather>
 __device__ __forceinline__ void o_mma(Smem& sm, const Unit& u, const SplitParams& p,
                                       uint32_t tmem, int lane) {
   const uint32_t ring = smem_u32(sm.ring);
@@ -665,7 +554,6 @@ __device__ __forceinline__ void o_mma(Smem& sm, const Unit& u, const SplitParams
     if (lane == 0 && j + 2 < u.ntiles) mbar_arrive_expect_tx(smem_u32(&sm.pfull[buf]), pbytes);
     fence_proxy_async_smem();
     if (!warp_wait(sm, smem_u32(&sm.vfull[slot]), (j >> 1) & 1, p, 12)) break;
-    if (kGather) fence_proxy_async_smem();   // rows written by cp.async, read by the MMA
     if (j == u.ntiles - 1 && u.zero_tail) {
       if (!o_command(sm, kCmdZeroTail | static_cast<uint32_t>(j), ncmd, p, lane)) break;
     }
@@ -821,10 +709,11 @@ __device__ __forceinline__ void o_helpers(Smem& sm, const Unit& u, const SplitPa
 
 // ============================================================ kernel
 
-// kGather: paged cache with pages that are not whole key tiles (rows gathered
-// with cp.async).  A separate instantiation keeps the gather code out of the
-// TMA kernel.
-template <bool kGather>
+// kAfterCopy: launched as a programmatic dependent of the grid that copied a
+// paged cache into a contiguous one; the cache loads first wait for that grid
+// (a separate instantiation: the wait instruction in the kernel cost ~0.7 us
+// per call even when not executed).
+template <bool kAfterCopy>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     verify_split_kernel(const __grid_constant__ CUtensorMap map_qn,
                         const __grid_constant__ CUtensorMap map_qr,
@@ -842,14 +731,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   const Unit u = decode_unit(p);
   // The slice merge is launched as a programmatic dependent of this grid; it
   // may be scheduled now and waits for this grid's completion itself.
-  if (tid == 0) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  if (tid == 0) grid_launch_dependents();
 
   if (tid == 0) {
     if ((u.S < p.q || u.S > p.Smax) && role == 0 && u.sp == 0 && u.rt == 0)
       atomicOr(p.status, kStatusSeqLen);
     for (int i = 0; i < kKSlots; ++i) {
       for (int part = 0; part < 2; ++part) {
-        mbar_init(smem_u32(&sm.kfull[part][i]), kGather ? kGatherThreads : 1);
+        mbar_init(smem_u32(&sm.kfull[part][i]), 1);
         mbar_init(smem_u32(&sm.kempty[part][i]), 1);
       }
     }
@@ -860,7 +749,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       mbar_init(smem_u32(&sm.sempty[i]), 8);
       mbar_init(smem_u32(&sm.pempty[i]), 1);
       mbar_init(smem_u32(&sm.pfull[i]), 1);
-      mbar_init(smem_u32(&sm.vfull[i]), kGather ? kGatherThreads : 1);
+      mbar_init(smem_u32(&sm.vfull[i]), 1);
       mbar_init(smem_u32(&sm.vempty[i]), 1);
     }
     mbar_init(smem_u32(&sm.odone), 1);
@@ -890,26 +779,22 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   const uint32_t tmem = sm.tmem_base;
 
   if (!u.empty) {
-    const bool gatherer = kGather && (warp == 0 || warp == 2 || warp == 3);
-    const int g = (warp == 0 ? 0 : warp - 1) * 32 + lane;   // gather thread index
     if (role == 0) {
-      if (gatherer) {
-        if constexpr (kGather) s_gather_producer(sm, u, p, &map_qn, &map_qr, g);
-      } else if (warp == 0 && lane == 0) {
+      if (warp == 0 && lane == 0) {
         tma_prefetch_desc(&map_qn);
         tma_prefetch_desc(&map_qr);
         tma_prefetch_desc(&map_kvs0);
         tma_prefetch_desc(&map_kvs1);
         int n_issued[2] = {0, 0};
         if (p.block_table != nullptr)
-          s_producer<true>(sm, u, p, &map_qn, &map_qr, &map_kvs0, &map_kvs1, n_issued);
+          s_producer<true, kAfterCopy>(sm, u, p, &map_qn, &map_qr, &map_kvs0, &map_kvs1, n_issued);
         else
-          s_producer<false>(sm, u, p, &map_qn, &map_qr, &map_kvs0, &map_kvs1, n_issued);
+          s_producer<false, kAfterCopy>(sm, u, p, &map_qn, &map_qr, &map_kvs0, &map_kvs1, n_issued);
         mbar_wait(smem_u32(&sm.qfull), 0, kWaitNs / 2);
         drain_ring(sm.kfull[0], kKSlots, n_issued[0]);
         drain_ring(sm.kfull[1], kKSlots, n_issued[1]);
       } else if (warp == 1) {
-        s_mma<kGather>(sm, u, p, tmem);
+        s_mma(sm, u, p, tmem);
         mma_commit_elect(smem_u32(&sm.drain));
         mbar_wait(smem_u32(&sm.drain), 0, kWaitNs);
         __syncwarp();
@@ -920,19 +805,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           s_softmax<false>(sm, u, p, tmem, warp & 3, (warp - 4) >> 2, lane);
       }
     } else {
-      if (gatherer) {
-        if constexpr (kGather) o_gather_producer(sm, u, p, g);
-      } else if (warp == 0 && lane == 0) {
+      if (warp == 0 && lane == 0) {
         tma_prefetch_desc(&map_kvo);
         tma_prefetch_desc(&map_out);
         int n_issued = 0;
         if (p.block_table != nullptr)
-          o_producer<true>(sm, u, p, &map_kvo, n_issued);
+          o_producer<true, kAfterCopy>(sm, u, p, &map_kvo, n_issued);
         else
-          o_producer<false>(sm, u, p, &map_kvo, n_issued);
+          o_producer<false, kAfterCopy>(sm, u, p, &map_kvo, n_issued);
         drain_ring(sm.vfull, kVSlots, n_issued);
       } else if (warp == 1) {
-        o_mma<kGather>(sm, u, p, tmem, lane);
+        o_mma(sm, u, p, tmem, lane);
         mma_commit_elect(smem_u32(&sm.drain));
         mbar_wait(smem_u32(&sm.drain), 0, kWaitNs);
         __syncwarp();

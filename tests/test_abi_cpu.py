@@ -116,6 +116,13 @@ def test_paged_host_argument_checks(lib):
     assert paged(lib, q=0) == -2 and paged(lib, scale=float("nan")) == -9
 
 
+def test_paged_workspace_size_rejects_bad_arguments(lib):
+    # Arguments mla_verify_attn_paged rejects size no workspace (and without a
+    # GPU every size is 0: the plan depends on the device).
+    for mb, ps in ((0, 64), (5, 0), (1 << 18, 64), (1 << 24, 1)):
+        assert mva.paged_workspace_size(1, 9, 64, mb, ps) == 0, (mb, ps)
+
+
 def test_paged_layout_helper():
     from mla_verify_attention_gb300 import inputs as I
     case = I.make_case(I.Workload("t", 2, 3, 100, "chain", H=2), smax_align=64)

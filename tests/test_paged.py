@@ -3,8 +3,9 @@
 Each case lays a seeded cache out as a page pool (random page order, NaN in
 unused pages and past each stream's length) and compares the paged call with
 the oracle on the logical cache, at the same tolerances as the contiguous
-path; one case also checks that paged and contiguous calls agree bit for bit.
-Pages of a multiple of 64 keys take the TMA path, other sizes the row gather.
+path; two cases also check that paged and contiguous calls agree bit for bit.
+Pages of a multiple of 64 keys are read in place through the block table;
+other sizes are first copied into a contiguous cache in the workspace.
 """
 import numpy as np
 import pytest
@@ -53,7 +54,7 @@ def check(case, out, lse):
     (1, 9, 64, [700], 256),            # tiles inside larger pages, partial last page
     (3, 5, 8, [10, 900, 2000], 128),   # ragged streams
     (2, 33, 64, [300, 1500], 64),      # two mask words
-    # page sizes that are not whole key tiles: rows gathered with cp.async
+    # page sizes that are not whole key tiles: rows copied into the workspace first
     (1, 9, 64, [4096], 1),             # one row per page (scattered rows), split path
     (3, 5, 8, [10, 900, 2000], 16),    # ragged streams, 16-row pages
     (1, 33, 64, [700], 96),            # pages straddling key tiles
@@ -97,9 +98,9 @@ def test_paged_bad_block_entry_is_reported():
     assert mva.last_device_error() == 0
 
 
-def test_gathered_pages_equal_contiguous_bitwise():
-    """Page size 1: the gather fills the same tile layout, so the result is the
-    contiguous call's, bit for bit."""
+def test_copied_pages_equal_contiguous_bitwise():
+    """Page size 1: the split kernel reads a contiguous copy of the cache, so the
+    result is the contiguous call's, bit for bit."""
     import torch
     import mla_verify_attention_gb300 as mva
     case = I.make_case(I.WORKLOADS["tree9_p4096"])
@@ -110,3 +111,29 @@ def test_gathered_pages_equal_contiguous_bitwise():
                           _t(case.mask.view(np.int32), torch.int32), float(case.scale))
     torch.cuda.synchronize()
     assert torch.equal(out_p, ref[0]) and torch.equal(lse_p, ref[1])
+
+
+def test_paged_workspace_sizes():
+    import torch
+    import mla_verify_attention_gb300 as mva
+    B, q, H, mb = 2, 9, 64, 70
+    for ps in (64, 128):   # read in place: the contiguous call's workspace
+        assert mva.paged_workspace_size(B, q, H, mb, ps) == mva.workspace_size(B, q, H, mb * ps)
+    for ps in (1, 16, 96):  # plus the contiguous copy, after the partials at 256 bytes
+        part = mva.workspace_size(B, q, H, mb * ps)
+        assert mva.paged_workspace_size(B, q, H, mb, ps) == -(-part // 256) * 256 + B * mb * ps * 1152
+    # one byte short is refused before anything is enqueued
+    case = I.make_case(I.WORKLOADS["chain9_p256"])
+    pool, table = I.to_paged(case, 1, seed=3)
+    need = mva.paged_workspace_size(case.B, case.q, case.H, table.shape[1], 1)
+    ws = torch.empty(need, dtype=torch.uint8, device="cuda")
+    args = (_t(case.q_nope.view(np.int16), torch.bfloat16), _t(case.q_rope.view(np.int16), torch.bfloat16),
+            _t(pool.view(np.int16), torch.bfloat16), _t(table, torch.int32), 1,
+            _t(case.seq_lens, torch.int32), _t(case.mask.view(np.int32), torch.int32), float(case.scale))
+    with pytest.raises(mva.MLAError) as e:
+        mva.verify_attn_paged(*args, workspace=ws[:need - 1])
+    assert e.value.status == -4
+    out, lse = mva.verify_attn_paged(*args, workspace=ws)
+    torch.cuda.synchronize()
+    assert mva.last_device_error() == 0
+    check(case, out, lse)
