@@ -69,7 +69,12 @@ constexpr int kPHead = 1024;
 constexpr int kPBuf = kPHead + 2 * kPTerm;
 constexpr int kPOffset = kKSlots * kKTile;       // after the K ring / V tiles (144 KB)
 constexpr int kThreads = 384;                    // 12 warps: 4 control + 8 row warps
-constexpr int kRingBytes = kPOffset + 2 * kPBuf;
+// Q rows are staged (by TMA, then moved to tensor memory by the softmax warps)
+// behind key slot 0, so that key tile 0 can load at the same time as Q.
+constexpr int kQStage = kKTile;
+constexpr int kQBytes = kKChunks * kQChunk;     // 144 KB
+constexpr int kRingBytes = (kPOffset + 2 * kPBuf > kQStage + kQBytes) ? kPOffset + 2 * kPBuf
+                                                                      : kQStage + kQBytes;
 constexpr uint32_t kSoftmaxBar = 1;              // named barrier of the 8 softmax warps
 constexpr uint32_t kEpilogueBar = 2;             // O CTA: 2 and 3, one per half of the helpers
 constexpr int kOutBlock = kRows * 32 * 4;        // 16 KB: [128 rows][32 fp32 columns]
@@ -222,45 +227,77 @@ __device__ __forceinline__ void drain_ring(const uint64_t* full, int nslots, int
 
 // ============================================================ S CTA roles
 
+// Key tile j, part `part` (chunks 0..4 or 5..8) into its ring slot.
+__device__ __forceinline__ void s_issue_part(Smem& sm, const CUtensorMap* map_kv0,
+                                             const CUtensorMap* map_kv1, int2 org, int j, int part,
+                                             int* n_issued) {
+  const int slot = j % kKSlots;
+  const uint32_t full = smem_u32(&sm.kfull[part][slot]);
+  mbar_arrive_expect_tx(full, part ? kKPart1 : kKPart0);
+  tma_load_4d(smem_u32(sm.ring) + slot * kKTile + part * kKPart0, part ? map_kv1 : map_kv0, 0,
+              org.x, part ? kKSplit : 0, org.y, full);
+  n_issued[part] = j + 1;
+}
+
+// Thread 0, right after the barriers are initialised and before the CTA and
+// cluster syncs (~0.8 us): the Q rows of this unit (8 latent chunks + 1 rope
+// chunk of [128 rows x 64 dims], as boxes [8][128][64] of q_nope and [128][64]
+// of q_rope) and, unless the cache is a copy still being written by the
+// preceding grid, key tile 0 (slot 0 lies outside the Q staging area).
+template <bool kPaged, bool kAfterCopy>
+__device__ __forceinline__ void s_producer_start(Smem& sm, const Unit& u, const SplitParams& p,
+                                                 const CUtensorMap* map_qn, const CUtensorMap* map_qr,
+                                                 const CUtensorMap* map_kv0, const CUtensorMap* map_kv1,
+                                                 int* n_issued) {
+  tma_prefetch_desc(map_qn);
+  tma_prefetch_desc(map_qr);
+  tma_prefetch_desc(map_kv0);
+  tma_prefetch_desc(map_kv1);
+  const uint32_t qst = smem_u32(sm.ring) + kQStage;
+  const uint32_t qfull = smem_u32(&sm.qfull);
+  const int y = u.b * u.rows_total + u.row0;
+  mbar_arrive_expect_tx(qfull, kQBytes);
+  tma_load_3d(qst, map_qn, 0, y, 0, qfull);
+  tma_load_2d(qst + kVChunks * kQChunk, map_qr, 0, y, qfull);
+  if constexpr (!kAfterCopy) {
+    const int2 org = tile_origin<kPaged>(p, u, u.k0);
+    s_issue_part(sm, map_kv0, map_kv1, org, 0, 0, n_issued);
+    // Test hook: unit 0 never loads the second part of key tile 0.
+    if (!(p.test_stall && blockIdx.x == 0)) s_issue_part(sm, map_kv0, map_kv1, org, 0, 1, n_issued);
+  }
+}
+
+// The rest of the key tiles, after the syncs.  Two boxes per 64-key tile:
+// [5 chunks][64 keys][64 dims] and [4 chunks][64][64].  A part's buffer is
+// refilled as soon as the MMAs that read it are done, so the first chunks of
+// tile j+2 load while the last ones of tile j are used.  Tile origins are
+// looked up two tiles ahead (a block-table read for paged caches).
 template <bool kPaged, bool kAfterCopy>
 __device__ __forceinline__ void s_producer(Smem& sm, const Unit& u, const SplitParams& p,
-                                           const CUtensorMap* map_qn, const CUtensorMap* map_qr,
                                            const CUtensorMap* map_kv0, const CUtensorMap* map_kv1,
                                            int* n_issued) {
-  const uint32_t ring = smem_u32(sm.ring);
-  const uint32_t qfull = smem_u32(&sm.qfull);
-  // Q rows of this unit: 8 latent chunks + 1 rope chunk of [128 rows x 64 dims].
-  // Two boxes: [8 chunks][128 rows][64 dims] of q_nope and [128 rows][64] of q_rope.
-  const int y = u.b * u.rows_total + u.row0;
-  mbar_arrive_expect_tx(qfull, kKChunks * kQChunk);
-  tma_load_3d(ring, map_qn, 0, y, 0, qfull);
-  tma_load_2d(ring + kVChunks * kQChunk, map_qr, 0, y, qfull);
-  // The Q staging area overlaps the first ring slots: wait until the softmax
-  // warps have moved Q into tensor memory.
-  if (!wait_or_abort(sm, smem_u32(&sm.qready), 0, p, 1)) return;
   if (kAfterCopy) grid_dependency_wait();   // the cache is the preceding grid's copy
-  fence_proxy_async();
-  // Two boxes per 64-key tile: [5 chunks][64 keys][64 dims] and [4 chunks][64][64].
-  // A part's buffer is refilled as soon as the MMAs that read it are done, so
-  // the first chunks of tile j+2 load while the last ones of tile j are used.
-  // Tile origins are looked up two tiles ahead (a block-table read for paged caches).
-  int2 org0 = tile_origin<kPaged>(p, u, u.k0);
-  int2 org1 = u.ntiles > 1 ? tile_origin<kPaged>(p, u, u.k0 + kKeys) : org0;
-  for (int j = 0; j < u.ntiles; ++j) {
+  const int j0 = kAfterCopy ? 0 : 1;
+  // (Block-table entries are read only for tiles of the slice.)
+  int2 org0 = j0 < u.ntiles ? tile_origin<kPaged>(p, u, u.k0 + j0 * kKeys) : make_int2(0, 0);
+  int2 org1 = j0 + 1 < u.ntiles ? tile_origin<kPaged>(p, u, u.k0 + (j0 + 1) * kKeys) : org0;
+  for (int j = j0; j < u.ntiles; ++j) {
     const int2 org = org0;
     org0 = org1;
     if (j + 2 < u.ntiles) org1 = tile_origin<kPaged>(p, u, u.k0 + (j + 2) * kKeys);
+    if (j == 1) {
+      // Slot 1 lies in the Q staging area: wait until the softmax warps have
+      // moved Q into tensor memory.
+      if (!wait_or_abort(sm, smem_u32(&sm.qready), 0, p, 1)) return;
+      fence_proxy_async();
+    }
     const int slot = j % kKSlots;
 #pragma unroll
     for (int part = 0; part < 2; ++part) {
       if (p.test_stall && blockIdx.x == 0 && j == 0 && part == 1) continue;
       if (!wait_or_abort(sm, smem_u32(&sm.kempty[part][slot]), ((j / kKSlots) & 1) ^ 1, p, 2))
         return;
-      const uint32_t full = smem_u32(&sm.kfull[part][slot]);
-      mbar_arrive_expect_tx(full, part ? kKPart1 : kKPart0);
-      tma_load_4d(ring + slot * kKTile + part * kKPart0, part ? map_kv1 : map_kv0, 0, org.x,
-                  part ? kKSplit : 0, org.y, full);
-      n_issued[part] = j + 1;
+      s_issue_part(sm, map_kv0, map_kv1, org, j, part, n_issued);
     }
   }
 }
@@ -326,7 +363,7 @@ __device__ __forceinline__ void s_softmax(Smem& sm, const Unit& u, const SplitPa
   const bool qok = warp_wait(sm, smem_u32(&sm.qfull), 0, p, 6);
   if (named_bar_red_or(kSoftmaxBar, kRowThreads, !qok)) return;
   for (int c = half; c < kKChunks; c += 2) {
-    const uint8_t* src = sm.ring + c * kQChunk + r * 128;
+    const uint8_t* src = sm.ring + kQStage + c * kQChunk + r * 128;
     uint32_t v[32];
 #pragma unroll
     for (int q4 = 0; q4 < 8; ++q4) {
@@ -504,23 +541,43 @@ __device__ __forceinline__ void s_softmax(Smem& sm, const Unit& u, const SplitPa
 
 // ============================================================ O CTA roles
 
+// Value tile j into its ring slot.
+__device__ __forceinline__ void o_issue(Smem& sm, const CUtensorMap* map_kv, int2 org, int j,
+                                        int& n_issued) {
+  const int slot = j & 1;
+  const uint32_t full = smem_u32(&sm.vfull[slot]);
+  mbar_arrive_expect_tx(full, kVTile);
+  tma_load_4d(smem_u32(sm.ring) + slot * kVTile, map_kv, 0, org.x, 0, org.y, full);
+  n_issued = j + 1;
+}
+
+// Thread 0 before the syncs: value tiles 0 and 1 (both slots start empty),
+// unless the cache is a copy still being written by the preceding grid.
+template <bool kPaged, bool kAfterCopy>
+__device__ __forceinline__ void o_producer_start(Smem& sm, const Unit& u, const SplitParams& p,
+                                                 const CUtensorMap* map_kv, int& n_issued) {
+  tma_prefetch_desc(map_kv);
+  if constexpr (!kAfterCopy) {
+    for (int j = 0; j < 2 && j < u.ntiles; ++j)
+      o_issue(sm, map_kv, tile_origin<kPaged>(p, u, u.k0 + j * kKeys), j, n_issued);
+  }
+}
+
 template <bool kPaged, bool kAfterCopy>
 __device__ __forceinline__ void o_producer(Smem& sm, const Unit& u, const SplitParams& p,
                                            const CUtensorMap* map_kv, int& n_issued) {
-  const uint32_t ring = smem_u32(sm.ring);
   if (kAfterCopy) grid_dependency_wait();   // the cache is the preceding grid's copy
-  int2 org0 = tile_origin<kPaged>(p, u, u.k0);
-  int2 org1 = u.ntiles > 1 ? tile_origin<kPaged>(p, u, u.k0 + kKeys) : org0;
-  for (int j = 0; j < u.ntiles; ++j) {
+  const int j0 = kAfterCopy ? 0 : 2;
+  // (Block-table entries are read only for tiles of the slice.)
+  int2 org0 = j0 < u.ntiles ? tile_origin<kPaged>(p, u, u.k0 + j0 * kKeys) : make_int2(0, 0);
+  int2 org1 = j0 + 1 < u.ntiles ? tile_origin<kPaged>(p, u, u.k0 + (j0 + 1) * kKeys) : org0;
+  for (int j = j0; j < u.ntiles; ++j) {
     const int2 org = org0;
     org0 = org1;
     if (j + 2 < u.ntiles) org1 = tile_origin<kPaged>(p, u, u.k0 + (j + 2) * kKeys);
     const int slot = j & 1;
     if (!wait_or_abort(sm, smem_u32(&sm.vempty[slot]), ((j >> 1) & 1) ^ 1, p, 9)) return;
-    const uint32_t full = smem_u32(&sm.vfull[slot]);
-    mbar_arrive_expect_tx(full, kVTile);
-    tma_load_4d(ring + slot * kVTile, map_kv, 0, org.x, 0, org.y, full);
-    n_issued = j + 1;
+    o_issue(sm, map_kv, org, j, n_issued);
   }
 }
 
@@ -732,6 +789,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   // The slice merge is launched as a programmatic dependent of this grid; it
   // may be scheduled now and waits for this grid's completion itself.
   if (tid == 0) grid_launch_dependents();
+  int n_issued[2] = {0, 0};   // thread 0: tiles issued per ring part (S) / value tiles (O)
 
   if (tid == 0) {
     if ((u.S < p.q || u.S > p.Smax) && role == 0 && u.sp == 0 && u.rt == 0)
@@ -767,6 +825,21 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       mbar_arrive_expect_tx(smem_u32(&sm.mlfull), kRows * 8);
     }
     fence_mbarrier_init_cluster();
+    fence_proxy_async_smem();   // the initialised barriers, before TMA completes on them
+    if (!u.empty) {
+      if (role == 0) {
+        if (p.block_table != nullptr)
+          s_producer_start<true, kAfterCopy>(sm, u, p, &map_qn, &map_qr, &map_kvs0, &map_kvs1, n_issued);
+        else
+          s_producer_start<false, kAfterCopy>(sm, u, p, &map_qn, &map_qr, &map_kvs0, &map_kvs1, n_issued);
+      } else {
+        tma_prefetch_desc(&map_out);
+        if (p.block_table != nullptr)
+          o_producer_start<true, kAfterCopy>(sm, u, p, &map_kvo, n_issued[0]);
+        else
+          o_producer_start<false, kAfterCopy>(sm, u, p, &map_kvo, n_issued[0]);
+      }
+    }
   }
   if (!u.empty && warp == 2) {
     tmem_alloc(smem_u32(&sm.tmem_base), 512);
@@ -781,15 +854,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   if (!u.empty) {
     if (role == 0) {
       if (warp == 0 && lane == 0) {
-        tma_prefetch_desc(&map_qn);
-        tma_prefetch_desc(&map_qr);
-        tma_prefetch_desc(&map_kvs0);
-        tma_prefetch_desc(&map_kvs1);
-        int n_issued[2] = {0, 0};
         if (p.block_table != nullptr)
-          s_producer<true, kAfterCopy>(sm, u, p, &map_qn, &map_qr, &map_kvs0, &map_kvs1, n_issued);
+          s_producer<true, kAfterCopy>(sm, u, p, &map_kvs0, &map_kvs1, n_issued);
         else
-          s_producer<false, kAfterCopy>(sm, u, p, &map_qn, &map_qr, &map_kvs0, &map_kvs1, n_issued);
+          s_producer<false, kAfterCopy>(sm, u, p, &map_kvs0, &map_kvs1, n_issued);
         mbar_wait(smem_u32(&sm.qfull), 0, kWaitNs / 2);
         drain_ring(sm.kfull[0], kKSlots, n_issued[0]);
         drain_ring(sm.kfull[1], kKSlots, n_issued[1]);
@@ -806,14 +874,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       }
     } else {
       if (warp == 0 && lane == 0) {
-        tma_prefetch_desc(&map_kvo);
-        tma_prefetch_desc(&map_out);
-        int n_issued = 0;
         if (p.block_table != nullptr)
-          o_producer<true, kAfterCopy>(sm, u, p, &map_kvo, n_issued);
+          o_producer<true, kAfterCopy>(sm, u, p, &map_kvo, n_issued[0]);
         else
-          o_producer<false, kAfterCopy>(sm, u, p, &map_kvo, n_issued);
-        drain_ring(sm.vfull, kVSlots, n_issued);
+          o_producer<false, kAfterCopy>(sm, u, p, &map_kvo, n_issued[0]);
+        drain_ring(sm.vfull, kVSlots, n_issued[0]);
       } else if (warp == 1) {
         o_mma(sm, u, p, tmem, lane);
         mma_commit_elect(smem_u32(&sm.drain));
