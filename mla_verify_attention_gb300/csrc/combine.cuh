@@ -8,7 +8,10 @@
 // lse = (M + log2 L) ln 2.  Slices with l_s = 0 are skipped (their O_s is 0).
 //
 // Memory-bound: one 128-thread block per query row, 16-byte loads and stores,
-// fully coalesced over the 512-wide rows; up to 16 slices' loads in flight.
+// fully coalesced over the 512-wide rows; up to kBatch slices' loads in flight.
+// The batch follows the slice count (4, 8 or 16): a smaller batch takes fewer
+// registers, so more blocks (rows) are resident per SM, and a call with many
+// rows and few slices (many short streams) is not a train of short waves.
 #pragma once
 #include <cstdint>
 #include <math_constants.h>
@@ -28,16 +31,17 @@ struct CombineParams {
   int q, Smax, nsplit, chunk_keys;
 };
 
-constexpr int kCombineBatch = 16;   // slices whose loads are in flight together
-
 // Launched as a programmatic dependent of the split kernel: the block may start
 // while that grid still runs and waits here until its results are visible.
 __device__ __forceinline__ void wait_for_split_grid() {
   asm volatile("griddepcontrol.wait;" ::: "memory");
 }
 
-// Four blocks per SM (<= 128 registers): all rows of a 64-head, 9-draft call in one wave.
-__global__ void __launch_bounds__(128, 4) combine_kernel(const CombineParams p) {
+// kBatch 16: four blocks per SM (<= 128 registers), all rows of a 64-head,
+// 9-draft call in one wave; kBatch 8 and 4: 6 and 12 blocks per SM.
+template <int kBatch>
+__global__ void __launch_bounds__(128, kBatch == 16 ? 4 : (kBatch == 8 ? 6 : 12))
+    combine_kernel(const CombineParams p) {
   wait_for_split_grid();
   const int row = blockIdx.x;
   const int tid = threadIdx.x;
@@ -53,11 +57,11 @@ __global__ void __launch_bounds__(128, 4) combine_kernel(const CombineParams p) 
   // before any is used; batches are merged online (running max M).
   float M = -CUDART_INF_F, L = 0.f;
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-  for (int s0 = 0; s0 < ns; s0 += kCombineBatch) {
-    float2 v[kCombineBatch];
-    float4 o[kCombineBatch];
+  for (int s0 = 0; s0 < ns; s0 += kBatch) {
+    float2 v[kBatch];
+    float4 o[kBatch];
 #pragma unroll
-    for (int e = 0; e < kCombineBatch; ++e) {
+    for (int e = 0; e < kBatch; ++e) {
       const int s = s0 + e;
       if (s < ns) {
         v[e] = ml[static_cast<size_t>(s) * p.N];
@@ -69,13 +73,13 @@ __global__ void __launch_bounds__(128, 4) combine_kernel(const CombineParams p) 
     }
     float Mb = M;
 #pragma unroll
-    for (int e = 0; e < kCombineBatch; ++e) Mb = v[e].y > 0.f ? fmaxf(Mb, v[e].x) : Mb;
+    for (int e = 0; e < kBatch; ++e) Mb = v[e].y > 0.f ? fmaxf(Mb, v[e].x) : Mb;
     if (Mb == -CUDART_INF_F) continue;            // nothing visible so far
     const float c = ex2(M - Mb);                  // 0 while M = -inf (L, acc are 0 then)
     L *= c;
     acc.x *= c; acc.y *= c; acc.z *= c; acc.w *= c;
 #pragma unroll
-    for (int e = 0; e < kCombineBatch; ++e) {
+    for (int e = 0; e < kBatch; ++e) {
       const float w = v[e].y > 0.f ? ex2(v[e].x - Mb) : 0.f;
       L += w * v[e].y;
       acc.x += w * o[e].x;

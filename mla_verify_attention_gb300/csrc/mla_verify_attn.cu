@@ -426,7 +426,12 @@ int run(const Call& c) {
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = timing ? 0 : 1;   // an event between the launches: plain ordering
-    if (cudaLaunchKernelEx(&cfg, mla::combine_kernel, c) != cudaSuccess) {
+    // Slices per load batch: 16 while all rows fit one wave at four blocks per
+    // SM, else 8 (more resident rows; batches are merged online).
+    const int nb = ns <= 4 ? 4 : ((ns <= 8 || rows > 4LL * d->sms) ? 8 : 16);
+    if (cudaLaunchKernelEx(&cfg, nb == 4 ? mla::combine_kernel<4>
+                                 : (nb == 8 ? mla::combine_kernel<8> : mla::combine_kernel<16>),
+                           c) != cudaSuccess) {
       cudaGetLastError();
       return MLA_ERR_LAUNCH;
     }

@@ -138,17 +138,74 @@ struct Unit {
   bool empty, two_term, zero_tail;
 };
 
+// Streams up to which slices are started longest first (one lane per stream).
+constexpr int kOrderedStreams = 32;
+
+// Slice (stream b, index sp, stream length S_b) of the t-th slice in start
+// order, for B <= kOrderedStreams; b = -1 for the empty slices at the end.  Clusters start in
+// index order, so this is a list schedule: every stream's full-length slices
+// first (slice-major), then the streams' shorter last slices, longest first
+// (ties: lower stream first), so that the device does not end on a tail of
+// long slices started late.  Computed by each warp with one lane per stream.
+__device__ __forceinline__ void ordered_slice(const SplitParams& p, int t, int& b, int& sp, int& S_b) {
+  const int lane = threadIdx.x & 31;
+  int tiles = 0, S = 0;
+  if (lane < p.B) {
+    S = p.seq_lens[lane];
+    tiles = (S < p.q || S > p.Smax) ? 0 : (S + kKeys - 1) / kKeys;
+  }
+  const int full = tiles / p.chunk_tiles;
+  const int rem = tiles - full * p.chunk_tiles;
+  int base = 0;
+  for (int s = 0; s < p.nsplit; ++s) {
+    unsigned m = __ballot_sync(0xFFFFFFFFu, full > s);
+    const int n = __popc(m);
+    if (n == 0) break;
+    if (t < base + n) {
+      for (int i = 0; i < t - base; ++i) m &= m - 1;   // the (t - base)-th stream with a slice s
+      b = __ffs(m) - 1;
+      sp = s;
+      S_b = __shfl_sync(0xFFFFFFFFu, S, b);
+      return;
+    }
+    base += n;
+  }
+  t -= base;
+  int rank = 0;   // among the shorter last slices
+  for (int o = 0; o < 32; ++o) {
+    const int ro = __shfl_sync(0xFFFFFFFFu, rem, o);
+    rank += (ro > rem || (ro == rem && o < lane)) ? 1 : 0;
+  }
+  const unsigned hit = __ballot_sync(0xFFFFFFFFu, rem > 0 && rank == t);
+  const int src = hit ? __ffs(hit) - 1 : 0;
+  const int full_hit = __shfl_sync(0xFFFFFFFFu, full, src);
+  S_b = __shfl_sync(0xFFFFFFFFu, S, src);
+  b = hit ? src : -1;
+  sp = hit ? full_hit : 0;
+}
+
+// Called by every thread of the CTA (full warps) at kernel start.
 __device__ __forceinline__ Unit decode_unit(const SplitParams& p) {
   Unit u;
-  // Units are numbered slice-major (all streams' slice 0, then slice 1, ...):
-  // clusters start in index order, so full-length slices go first and the
-  // shorter last slices of streams (and empty ones past a stream's end) last.
+  // Each slice's n_rt row tiles are consecutive units (they read the same keys).
+  // For 2 to kOrderedStreams streams, slices start longest first
+  // (ordered_slice); otherwise slice-major (all streams' slice 0, then slice 1,
+  // ...), which for one stream is the same order.
   const int unit = blockIdx.x >> 1;
   u.rt = unit % p.n_rt;
   const int t = unit / p.n_rt;
-  u.b = t % p.B;
-  u.sp = t / p.B;
-  u.S = p.seq_lens[u.b];
+  int b, sp, S;
+  if (p.B > 1 && p.B <= kOrderedStreams) {
+    ordered_slice(p, t, b, sp, S);
+  } else {
+    b = t % p.B;
+    sp = t / p.B;
+    S = p.seq_lens[b];
+  }
+  const bool none = b < 0;   // an empty slice at the end of the order
+  u.b = none ? 0 : b;
+  u.sp = sp;
+  u.S = none ? p.q : S;
   u.prefix = u.S - p.q;
   u.rows_total = p.q * p.H;
   u.row0 = u.rt * kRows;
@@ -156,7 +213,7 @@ __device__ __forceinline__ Unit decode_unit(const SplitParams& p) {
   const bool bad = u.S < p.q || u.S > p.Smax;
   u.k0 = u.sp * p.chunk_tiles * kKeys;
   u.k1 = min(u.S, u.k0 + p.chunk_tiles * kKeys);
-  u.empty = bad || u.k0 >= u.k1;
+  u.empty = none || bad || u.k0 >= u.k1;
   u.ntiles = u.empty ? 0 : (u.k1 - u.k0 + kKeys - 1) / kKeys;
   u.two_term = u.S <= p.two_term_max_keys;
   u.zero_tail = !u.empty && ((u.k1 - u.k0) % kKeys) != 0;
@@ -792,8 +849,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   int n_issued[2] = {0, 0};   // thread 0: tiles issued per ring part (S) / value tiles (O)
 
   if (tid == 0) {
-    if ((u.S < p.q || u.S > p.Smax) && role == 0 && u.sp == 0 && u.rt == 0)
+    // A stream length outside [q, Smax] is reported once: by the unit of its
+    // slice 0 and row tile 0 (slice-major order), or by CTA 0 (ordered starts,
+    // which give such a stream no slices).
+    if (p.B > 1 && p.B <= kOrderedStreams) {
+      if (blockIdx.x == 0)
+        for (int b = 0; b < p.B; ++b)
+          if (p.seq_lens[b] < p.q || p.seq_lens[b] > p.Smax) atomicOr(p.status, kStatusSeqLen);
+    } else if ((u.S < p.q || u.S > p.Smax) && role == 0 && u.sp == 0 && u.rt == 0) {
       atomicOr(p.status, kStatusSeqLen);
+    }
     for (int i = 0; i < kKSlots; ++i) {
       for (int part = 0; part < 2; ++part) {
         mbar_init(smem_u32(&sm.kfull[part][i]), 1);

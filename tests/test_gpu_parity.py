@@ -116,6 +116,43 @@ def test_edge_shapes_split():
     check(case, *run_gpu(case, nsplit=4))
 
 
+@pytest.mark.parametrize("B,nsplit", [
+    (20, 5),    # slices start longest first: full slices, then last slices by length
+    (40, 3),    # more streams than lanes of a warp: slice-major starts
+])
+def test_many_ragged_streams(B, nsplit):
+    rng = np.random.default_rng(B)
+    prefixes = [int(x) for x in rng.integers(0, 700, B)]
+    case = custom_case(B, 3, 8, prefixes, seed=300 + B)
+    check(case, *run_gpu(case, nsplit=nsplit))
+    check(case, *run_gpu(case))
+
+
+@pytest.mark.parametrize("B", [3, 40])
+def test_bad_stream_length_is_reported(B):
+    # One stream claims more keys than Smax: MLA_ERR_SEQLEN once, and the other
+    # streams' results are unaffected.
+    import torch
+    import mla_verify_attention_gb300 as mva
+    prefixes = [100 + 37 * (i % 5) for i in range(B)]
+    case = custom_case(B, 3, 8, prefixes, seed=400 + B)
+    good_out, good_lse = run_gpu(case)
+    bad = case.seq_lens.copy()
+    bad[1] = case.Smax + 1
+    args = list(to_dev(case))
+    args[3] = torch.from_numpy(bad).to(args[3].device)
+    out, lse = mva.verify_attn(*args, float(case.scale))
+    torch.cuda.synchronize()
+    assert mva.last_device_error() == -8      # MLA_ERR_SEQLEN, then cleared
+    assert mva.last_device_error() == 0
+    rows = case.q * case.H
+    o = out.cpu().numpy().astype(np.float64).reshape(B, rows, 512)
+    l = lse.cpu().numpy().astype(np.float64).reshape(B, rows)
+    keep = [b for b in range(B) if b != 1]
+    np.testing.assert_array_equal(o[keep], good_out.reshape(B, rows, 512)[keep])
+    np.testing.assert_array_equal(l[keep], good_lse.reshape(B, rows)[keep])
+
+
 def test_empty_rows_are_zero_and_minus_inf():
     case = custom_case(1, 4, 64, [0], seed=9, tree="chain")
     case.mask[0, 0, 0] = 0          # draft 0 sees nothing at all
