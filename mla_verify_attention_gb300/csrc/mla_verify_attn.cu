@@ -26,7 +26,7 @@ constexpr int kMaxDevices = 64;
 // (Q load, epilogue) and adds a partial to merge.  Measured on tree9/chain9
 // shapes: 2-tile slices beat longer ones while all units fit one wave.
 constexpr int kMinTilesPerSlice = 2;
-constexpr int kTwoTermMaxKeys = 4096;         // streams up to this length send P as hi + lo
+constexpr int kTwoTermMaxKeys = 32768;        // streams up to this length send P as hi + lo
 constexpr size_t kSmemBytes = sizeof(mla::Smem) + 1024;   // + manual 1 KB alignment
 
 struct DeviceInfo {

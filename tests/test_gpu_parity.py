@@ -153,6 +153,18 @@ def test_bad_stream_length_is_reported(B):
     np.testing.assert_array_equal(l[keep], good_lse.reshape(B, rows)[keep])
 
 
+@pytest.mark.parametrize("S,seed", [(2100, 1700 + 31 * 4 + 2100), (12000, 1700 + 31 * 3 + 12000),
+                                    (4105, 4105), (32760, 77), (32800, 78)])
+def test_precision_across_stream_lengths(S, seed):
+    # Inputs on which bf16 P in one term missed the tolerance (4.8e-3 at 2100
+    # keys, 2.4e-3 at 12000): with a lazily updated row max, even the dominant
+    # key's weight carries the bf16 rounding error.  Streams up to 32768 keys
+    # send P as two terms; at 32800 one term stays well inside (~6e-4).
+    w = I.Workload("custom", 1, 9, 0, "random", 5, None, H=64, index=0)
+    case = I.make_case(w, seed=seed, prefixes=[S - 9])
+    check(case, *run_gpu(case))
+
+
 def test_empty_rows_are_zero_and_minus_inf():
     case = custom_case(1, 4, 64, [0], seed=9, tree="chain")
     case.mask[0, 0, 0] = 0          # draft 0 sees nothing at all
