@@ -426,7 +426,7 @@ def run_ours(args, rank, world, local_rank):
     roof["traffic"] = recorded_traffic(args.workload)
     roof["peak_source"] = "%s (MEASURED_PEAKS.json burst)" % peak_src if peak_src == "measured" \
         else "fallback"
-    roof["kernel"] = "verify_split_kernel (%d launches per call)" % launches_per_call
+    roof["kernel"] = "verify_split_kernel (1 of %d launches per call)" % launches_per_call
     roof["kernel_us"] = split_us
     roof["call_us"] = us_call
     roof["call_frac"] = (flops / (us_call * 1e-6) / 1e12) / bf16_tf if t_tensor >= t_hbm else \
