@@ -301,7 +301,9 @@ def run_ours(args, rank, world, local_rank):
     # split kernel, the slice merge when the keys are split, and for pages
     # that are not whole 64-key tiles the copy into a contiguous cache
     copied = paged and args.page_size % 64 != 0
-    launches_per_call = 1 + (1 if nsplit > 1 else 0) + (1 if copied else 0)
+    # the library's planner kernel: split calls with 2..32 streams, slice count not forced
+    planned = 2 <= B <= 32 and 1 < nsplit <= 32 and int(os.environ.get("MLA_VERIFY_NSPLIT", "0") or 0) <= 0
+    launches_per_call = 1 + (1 if nsplit > 1 else 0) + (1 if copied else 0) + (1 if planned else 0)
     stream = torch.cuda.current_stream(dev)
     sh = int(stream.cuda_stream)
     ptrs = [q_nope.data_ptr(), q_rope.data_ptr(), None, seq.data_ptr(), mask.data_ptr()]

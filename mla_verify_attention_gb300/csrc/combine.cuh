@@ -29,6 +29,7 @@ struct CombineParams {
   int N;                   // B * q * H rows
   int rows_per_stream;     // q * H
   int q, Smax, nsplit, chunk_keys;
+  const int* plan;         // device-side {chunk_tiles, nsplit}, or null (the fields above)
 };
 
 // Launched as a programmatic dependent of the split kernel: the block may start
@@ -48,7 +49,8 @@ __global__ void __launch_bounds__(128, kBatch == 16 ? 4 : (kBatch == 8 ? 6 : 12)
   const int b = row / p.rows_per_stream;
   const int S = p.seq_lens[b];
   if (S < p.q || S > p.Smax) return;   // reported by the split kernel
-  const int ns = min(p.nsplit, (S + p.chunk_keys - 1) / p.chunk_keys);
+  const int chunk_keys = p.plan != nullptr ? p.plan[0] * 64 : p.chunk_keys;
+  const int ns = min(p.plan != nullptr ? p.plan[1] : p.nsplit, (S + chunk_keys - 1) / chunk_keys);
   const float2* ml = p.part_ml + row;
   const float4* src = reinterpret_cast<const float4*>(p.part_o + static_cast<size_t>(row) * 512) + tid;
   const size_t step4 = static_cast<size_t>(p.N) * 128;   // float4s between slices

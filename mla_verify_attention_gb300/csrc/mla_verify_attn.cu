@@ -14,6 +14,7 @@
 #include "combine.cuh"
 #include "verify_split.cuh"
 #include "repack.cuh"
+#include "planner.cuh"
 
 namespace {
 
@@ -22,10 +23,11 @@ namespace {
 __device__ unsigned int g_mla_status;
 
 constexpr int kMaxDevices = 64;
-// Shortest slice: a slice of a short stream still pays the unit's fixed cost
-// (Q load, epilogue) and adds a partial to merge.  Measured on tree9/chain9
-// shapes: 2-tile slices beat longer ones while all units fit one wave.
-constexpr int kMinTilesPerSlice = 2;
+// Shortest slice (mla::kMinSliceTiles): a slice of a short stream still pays
+// the unit's fixed cost (Q load, epilogue) and adds a partial to merge.
+// Measured on tree9/chain9 shapes: 2-tile slices beat longer ones while all
+// units fit one wave.
+constexpr int kMinTilesPerSlice = mla::kMinSliceTiles;
 constexpr int kTwoTermMaxKeys = 32768;        // streams up to this length send P as hi + lo
 constexpr size_t kSmemBytes = sizeof(mla::Smem) + 1024;   // + manual 1 KB alignment
 
@@ -140,10 +142,27 @@ int plan(int B, int q, int H, int Smax, int max_clusters, int* n_rt, int* nsplit
   return MLA_OK;
 }
 
+// Split calls: [nsplit][B*q*H][512] fp32 accumulators, [nsplit][B*q*H] (max, sum)
+// pairs, then (at a 256-byte boundary) 256 bytes for the device-side plan.
+size_t plan_offset(int B, int q, int H, int nsplit) {
+  const size_t n = static_cast<size_t>(B) * q * H;
+  const size_t end = static_cast<size_t>(nsplit) * n * (512 * sizeof(float) + sizeof(float2));
+  return (end + 255) & ~static_cast<size_t>(255);
+}
 size_t workspace_bytes_for(int B, int q, int H, int nsplit) {
   if (nsplit <= 1) return 0;
-  const size_t n = static_cast<size_t>(B) * q * H;
-  return static_cast<size_t>(nsplit) * n * (512 * sizeof(float) + sizeof(float2));
+  return plan_offset(B, q, H, nsplit) + 256;
+}
+
+bool nsplit_forced() {
+  const char* env = std::getenv("MLA_VERIFY_NSPLIT");
+  return env && std::atoll(env) > 0;
+}
+
+// Calls whose slice count plan_kernel chooses from the stream lengths: split
+// calls with 2 to 32 streams, unless the count is forced.
+bool device_planned(int B, int nsplit) {
+  return B >= 2 && B <= mla::kOrderedStreams && nsplit > 1 && !nsplit_forced();
 }
 
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
@@ -346,6 +365,11 @@ int run(const Call& c) {
   p.n_rt = nrt;
   p.nsplit = ns;
   p.chunk_tiles = ct;
+  const bool planned = device_planned(B, ns);
+  int* const plan_dev = planned ? reinterpret_cast<int*>(static_cast<char*>(workspace) +
+                                                         plan_offset(B, q_len, H, ns))
+                                : nullptr;
+  p.plan = plan_dev;
   p.two_term_max_keys = kTwoTermMaxKeys;
   const char* stall = std::getenv("MLA_VERIFY_TEST_STALL");
   p.test_stall = (stall && stall[0] && stall[0] != '0') ? 1 : 0;
@@ -372,10 +396,27 @@ int run(const Call& c) {
     mla::repack_kernel<<<grid, mla::kRepackThreads, 0, stream>>>(rp);
     if (cudaGetLastError() != cudaSuccess) return MLA_ERR_LAUNCH;
   }
+  if (planned) {
+    mla::PlanParams pp;
+    pp.seq_lens = seq_lens;
+    pp.plan = plan_dev;
+    pp.B = B;
+    pp.q = q_len;
+    pp.Smax = Smax;
+    pp.n_rt = nrt;
+    pp.nsplit_max = ns;
+    pp.min_chunk = kMinTilesPerSlice;
+    pp.slots = d->max_clusters;
+    pp.two_term_max_keys = kTwoTermMaxKeys;
+    const int ncand = ns < mla::kPlanMaxCandidates ? ns : mla::kPlanMaxCandidates;
+    mla::plan_kernel<<<1, 32 * ncand, 0, stream>>>(pp);
+    if (cudaGetLastError() != cudaSuccess) return MLA_ERR_LAUNCH;
+  }
   const bool timing = g_timing_before != nullptr;
   // After the cache copy the split kernel is its programmatic dependent
-  // (prologue overlapped, cache loads wait for the copy to complete).
-  const bool after_copy = copy && !timing;
+  // (prologue overlapped, cache loads wait for the copy to complete); after
+  // the planner it starts in plain stream order (its units follow the plan).
+  const bool after_copy = copy && !timing && !planned;
   if (timing && cudaEventRecord(g_timing_before, stream) != cudaSuccess) {
     cudaGetLastError();
     return MLA_ERR_LAUNCH;
@@ -414,6 +455,7 @@ int run(const Call& c) {
     c.Smax = Smax;
     c.nsplit = ns;
     c.chunk_keys = ct * mla::kKeys;
+    c.plan = plan_dev;
     // Programmatic dependent launch: the merge blocks may be scheduled while
     // the split kernel drains and wait (griddepcontrol.wait) for its results.
     cudaLaunchConfig_t cfg = {};

@@ -111,6 +111,10 @@ struct SplitParams {
   // Test hook (MLA_VERIFY_TEST_STALL): unit 0 never loads the second part of
   // key tile 0, so its bounded waits run out and report MLA_ERR_DEVICE_TIMEOUT.
   int test_stall;
+  // Calls with 2..kOrderedStreams streams: {chunk_tiles, nsplit} chosen by
+  // plan_kernel from the stream lengths (null: the host's values hold).  nsplit
+  // above stays the host's (grid, workspace, partials or direct output).
+  const int* plan;
 };
 
 struct __align__(1024) Smem {
@@ -140,6 +144,7 @@ struct Unit {
 
 // Streams up to which slices are started longest first (one lane per stream).
 constexpr int kOrderedStreams = 32;
+constexpr int kMinSliceTiles = 2;   // shortest slice: a unit's fixed cost needs a few tiles
 
 // Slice (stream b, index sp, stream length S_b) of the t-th slice in start
 // order, for B <= kOrderedStreams; b = -1 for the empty slices at the end.  Clusters start in
@@ -147,15 +152,16 @@ constexpr int kOrderedStreams = 32;
 // first (slice-major), then the streams' shorter last slices, longest first
 // (ties: lower stream first), so that the device does not end on a tail of
 // long slices started late.  Computed by each warp with one lane per stream.
-__device__ __forceinline__ void ordered_slice(const SplitParams& p, int t, int& b, int& sp, int& S_b) {
+__device__ __forceinline__ void ordered_slice(const SplitParams& p, int chunk, int t, int& b, int& sp,
+                                              int& S_b) {
   const int lane = threadIdx.x & 31;
   int tiles = 0, S = 0;
   if (lane < p.B) {
     S = p.seq_lens[lane];
     tiles = (S < p.q || S > p.Smax) ? 0 : (S + kKeys - 1) / kKeys;
   }
-  const int full = tiles / p.chunk_tiles;
-  const int rem = tiles - full * p.chunk_tiles;
+  const int full = tiles / chunk;
+  const int rem = tiles - full * chunk;
   int base = 0;
   for (int s = 0; s < p.nsplit; ++s) {
     unsigned m = __ballot_sync(0xFFFFFFFFu, full > s);
@@ -195,8 +201,10 @@ __device__ __forceinline__ Unit decode_unit(const SplitParams& p) {
   u.rt = unit % p.n_rt;
   const int t = unit / p.n_rt;
   int b, sp, S;
+  int chunk = p.chunk_tiles;
   if (p.B > 1 && p.B <= kOrderedStreams) {
-    ordered_slice(p, t, b, sp, S);
+    if (p.plan != nullptr) chunk = p.plan[0];   // the slice length plan_kernel chose
+    ordered_slice(p, chunk, t, b, sp, S);
   } else {
     b = t % p.B;
     sp = t / p.B;
@@ -211,8 +219,8 @@ __device__ __forceinline__ Unit decode_unit(const SplitParams& p) {
   u.row0 = u.rt * kRows;
   u.valid_rows = min(kRows, u.rows_total - u.row0);
   const bool bad = u.S < p.q || u.S > p.Smax;
-  u.k0 = u.sp * p.chunk_tiles * kKeys;
-  u.k1 = min(u.S, u.k0 + p.chunk_tiles * kKeys);
+  u.k0 = u.sp * chunk * kKeys;
+  u.k1 = min(u.S, u.k0 + chunk * kKeys);
   u.empty = none || bad || u.k0 >= u.k1;
   u.ntiles = u.empty ? 0 : (u.k1 - u.k0 + kKeys - 1) / kKeys;
   u.two_term = u.S <= p.two_term_max_keys;
