@@ -84,3 +84,38 @@ def test_graph_replay_matches_eager_and_follows_new_inputs():
     ref_out, ref_lse = mva.verify_attn(*inputs, scale)
     torch.cuda.synchronize()
     assert torch.equal(out, ref_out) and torch.equal(lse, ref_lse)
+
+
+def test_graph_replay_with_device_plan_follows_new_stream_lengths():
+    # Several streams: the slice count is chosen on the device from seq_lens
+    # (a planner launch inside the captured sequence), so replays with other
+    # lengths re-plan and stay exact.
+    import torch
+    import mla_verify_attention_gb300 as mva
+    prefixes_a = [3000, 400, 1500, 6000]
+    prefixes_b = [200, 5900, 100, 900]
+    w = I.Workload("custom", 4, 9, 0, "random", 5, None, H=64, index=0)
+    case_a = I.make_case(w, seed=71, prefixes=prefixes_a)
+    case_b = I.make_case(w, seed=72, prefixes=prefixes_b, smax_align=case_a.Smax)
+    assert case_b.Smax == case_a.Smax
+    B, q, H, Smax, scale = case_a.B, case_a.q, case_a.H, case_a.Smax, float(case_a.scale)
+    assert mva.plan(B, q, H, Smax)[1] > 1
+
+    inputs = _dev(case_a)
+    out = torch.empty((B, q, H, 512), dtype=torch.float32, device="cuda")
+    lse = torch.empty((B, q, H), dtype=torch.float32, device="cuda")
+    ws = torch.empty(mva.workspace_size(B, q, H, Smax), dtype=torch.uint8, device="cuda")
+    mva.verify_attn(*inputs, scale, out=out, lse=lse, workspace=ws)
+    torch.cuda.synchronize()
+
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        mva.verify_attn(*inputs, scale, out=out, lse=lse, workspace=ws)
+    for case in (case_a, case_b, case_a):
+        for dst, src in zip(inputs, _dev(case)):
+            dst.copy_(src)
+        out.fill_(float("nan"))
+        graph.replay()
+        torch.cuda.synchronize()
+        assert mva.last_device_error() == 0
+        _check(case, out, lse)
