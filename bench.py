@@ -308,16 +308,17 @@ def run_ours(args, rank, world, local_rank):
     sh = int(stream.cuda_stream)
     ptrs = [q_nope.data_ptr(), q_rope.data_ptr(), None, seq.data_ptr(), mask.data_ptr()]
 
-    def call(i):
+    def call(i, stream_handle=None):
+        sh_i = sh if stream_handle is None else stream_handle
         if paged:
             st = mva.load_library().mla_verify_attn_paged(
                 ptrs[0], ptrs[1], kvs[i % copies].data_ptr(), kv0.shape[0], table_d.data_ptr(),
                 table_d.shape[1], args.page_size, ptrs[3], ptrs[4], B, q, H, float(case.scale),
-                out.data_ptr(), lse.data_ptr(), ws.data_ptr(), ws.numel(), sh)
+                out.data_ptr(), lse.data_ptr(), ws.data_ptr(), ws.numel(), sh_i)
         else:
             st = mva.verify_attn_raw(ptrs[0], ptrs[1], kvs[i % copies].data_ptr(), ptrs[3], ptrs[4],
                                      B, q, H, Smax, float(case.scale), out.data_ptr(),
-                                     lse.data_ptr(), ws.data_ptr(), ws.numel(), sh)
+                                     lse.data_ptr(), ws.data_ptr(), ws.numel(), sh_i)
         if st != 0:
             raise mva.MLAError(st)
 
@@ -372,6 +373,33 @@ def run_ours(args, rank, world, local_rank):
         mva.set_timing_events()
     torch.cuda.synchronize(dev)
     split_us = sum(a.elapsed_time(b) for a, b in split_evs) * 1e3 / n_split
+
+    # ---- the same calls replayed from a CUDA graph (one call per cache copy
+    # captured once): what a decode loop that captures its steps sees.  Context
+    # only; `value` above is stream-launched calls.
+    graph = torch.cuda.CUDAGraph()
+    gstream = torch.cuda.Stream(dev)
+    gstream.wait_stream(stream)
+    with torch.cuda.stream(gstream):
+        with torch.cuda.graph(graph, stream=gstream):
+            for i in range(copies):
+                call(i, int(gstream.cuda_stream))
+    torch.cuda.synchronize(dev)
+    reps = max(1, min(args.steps, 500) // copies)
+    graph.replay()
+    torch.cuda.synchronize(dev)
+    g0 = torch.cuda.Event(enable_timing=True)
+    g1 = torch.cuda.Event(enable_timing=True)
+    g0.record(stream)
+    for _ in range(reps):
+        graph.replay()
+    g1.record(stream)
+    torch.cuda.synchronize(dev)
+    graph_us = g0.elapsed_time(g1) * 1e3 / (reps * copies)
+    st = mva.last_device_error()
+    if st != 0:
+        raise mva.MLAError(st, "graph replay")
+    del graph
 
     # ---- end to end through the public API, from pinned host buffers
     host_in = [torch.from_numpy(np.ascontiguousarray(a)).pin_memory() for a in
@@ -461,6 +489,8 @@ def run_ours(args, rank, world, local_rank):
                                     "(RTX PRO 6000, fp32), context only" % ref) if ref else None}),
             "roofline": roof,
             "cpu_baseline": cpu,
+            "graph": {"us_per_call": graph_us, "calls": reps * copies,
+                      "what": "the same calls replayed from one captured CUDA graph (context)"},
             "e2e": {"value": e2e_us, "unit": UNIT, "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h},
             "gpu_launches": args.steps * launches_per_call,
