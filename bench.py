@@ -206,6 +206,20 @@ def oracle_sample(case, budget_s, steps=1):
     return us, cores, what, times
 
 
+def oracle_single_thread(case, budget_s):
+    """The oracle on one host thread, on as many query rows as fit the budget;
+    returns (us per full call, rows timed)."""
+    import oracle
+    rows = case.B * case.q * case.H
+    t0 = time.perf_counter()
+    oracle.case_reference(case, nthreads=1, rows=(0, 1))
+    per_row = time.perf_counter() - t0
+    n = max(1, min(rows, int(budget_s / max(per_row, 1e-9))))
+    t0 = time.perf_counter()
+    oracle.case_reference(case, nthreads=1, rows=(0, n))
+    return (time.perf_counter() - t0) * rows / n * 1e6, n
+
+
 # ----------------------------------------------------------------------- arms
 
 def run_reference(args, rank):
@@ -466,7 +480,10 @@ def run_ours(args, rank, world, local_rank):
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         c_us, cores, what, _ = oracle_sample(case, args.cpu_budget_s)
-        cpu = {"value": c_us, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": what}
+        s_us, s_rows = oracle_single_thread(case, min(5.0, args.cpu_budget_s / 4))
+        cpu = {"value": c_us, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": what,
+               "single_thread": {"value": s_us, "unit": UNIT,
+                                 "sample": "%d query rows on one thread, scaled to the whole call" % s_rows}}
 
     if rank == 0:
         ref = PAGES_US.get(args.workload)
