@@ -72,7 +72,10 @@ enum mla_status {
  * Scratch holds the per-split partial states of the key-range split (page
  * "The Decisive Microbench: When Theory Meets Silicon", section "The KV-Split
  * Solution"): [nsplit][B*q_len*H][512] fp32 accumulators followed by
- * [nsplit][B*q_len*H][2] fp32 (running max, running sum).
+ * [nsplit][B*q_len*H][2] fp32 (running max, running sum), then, at a
+ * 256-byte boundary, 256 bytes where calls with 2 to 32 streams keep the
+ * slice plan the device chose from seq_lens (a smaller slice count than the
+ * host's nsplit when the streams are ragged).
  */
 size_t mla_verify_attn_workspace_size(int B, int q_len, int H, int Smax);
 
@@ -175,7 +178,10 @@ const char* mla_verify_attn_strerror(int status);
  * `max_clusters` is the number of 2-CTA clusters that fit on the device at
  * once (pass <= 0 to query the current device).  Honours the environment
  * variable MLA_VERIFY_NSPLIT (a positive integer forces the slice count, for
- * testing the split path on small inputs).  Returns MLA_OK or a status.
+ * testing the split path on small inputs).  For 2 to 32 streams (count not
+ * forced) this is the largest plan: the call's first kernel may choose fewer
+ * slices from the device's seq_lens, and the slices then start longest first.
+ * Returns MLA_OK or a status.
  */
 int mla_verify_attn_plan(int B, int q_len, int H, int Smax, int max_clusters, int* n_row_tiles,
                          int* nsplit, int* chunk_tiles);

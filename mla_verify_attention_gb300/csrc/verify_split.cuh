@@ -33,9 +33,15 @@
 //
 // Each CTA streams the cache slice it needs with TMA (128-byte swizzle), from
 // a contiguous cache or from pages of a multiple of 64 keys (caches with other
-// page sizes are first copied into a contiguous one, see repack.cuh).  P is rounded to bf16 because V is bf16 in the cache; for
-// short streams (where a few keys carry most of the weight) P is sent as two
-// bf16 terms hi + lo and the PV product is issued once per term.
+// page sizes are first copied into a contiguous one, see repack.cuh).  P is
+// rounded to bf16 because V is bf16 in the cache.  With the lazily kept row
+// max even the dominant key's p carries that rounding, so streams up to
+// two_term_max_keys keys (where a few keys carry most of the weight) send P as
+// two bf16 terms hi + lo and the PV product is issued once per term.
+//
+// Units start in index order.  For 2..32 streams the index order is a list
+// schedule (ordered_slice), and the slice length may come from plan_kernel
+// (planner.cuh), which chose it from the stream lengths.
 #pragma once
 #include <cstdint>
 #include <cstdio>
