@@ -26,6 +26,7 @@ import hashlib
 import json
 import math
 import os
+import re
 import statistics
 import subprocess
 import sys
@@ -81,12 +82,21 @@ def measured_peaks():
         return 6800.0, 1900.0, "fallback"
 
 
-def kernel_src_hash():
+def _code_tokens(text):
+    """Source text without comments and with whitespace collapsed: edits to
+    comments alone leave the hash (and the recorded traffic) valid."""
+    text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", " ", text)
+    return " ".join(text.split())
+
+
+def kernel_src_hash(csrc=None):
+    """sha256/16 of the CUDA sources' code (comments and layout ignored)."""
     h = hashlib.sha256()
-    csrc = os.path.join(ROOT, "mla_verify_attention_gb300", "csrc")
+    csrc = csrc or os.path.join(ROOT, "mla_verify_attention_gb300", "csrc")
     for fn in sorted(os.listdir(csrc)):
-        with open(os.path.join(csrc, fn), "rb") as fh:
-            h.update(fn.encode() + fh.read())
+        with open(os.path.join(csrc, fn), encoding="utf-8") as fh:
+            h.update(fn.encode() + _code_tokens(fh.read()).encode())
     return h.hexdigest()[:16]
 
 
