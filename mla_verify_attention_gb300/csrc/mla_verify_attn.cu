@@ -124,12 +124,13 @@ int plan(int B, int q, int H, int Smax, int max_clusters, int* n_rt, int* nsplit
     ns = forced < tiles ? forced : tiles;
     ct = static_cast<int>((tiles + ns - 1) / ns);
   } else {
-    if (base >= max_clusters) {
-      ns = 1;
-    } else if (B <= 1) {
-      ns = max_clusters / base;                       // one wave of clusters
+    if (B <= 1) {
+      ns = base >= max_clusters ? 1 : max_clusters / base;   // one wave of clusters
     } else {
-      ns = (4LL * max_clusters + base - 1) / base;    // ragged streams: smaller slices
+      // Several streams (of unknown, possibly ragged lengths): about four
+      // waves' worth of slices, so that long streams are cut up even when the
+      // streams alone fill a wave; the device refines the count (planner.cuh).
+      ns = (4LL * max_clusters + base - 1) / base;
     }
     ct = static_cast<int>((tiles + ns - 1) / ns);
     if (ct < kMinTilesPerSlice) ct = kMinTilesPerSlice;

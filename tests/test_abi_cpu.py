@@ -81,6 +81,9 @@ def test_plan_arithmetic(lib):
     # ragged batch: smaller slices for balance
     nrt, ns, ct = mva.plan(8, 9, 64, 32832, 76)
     assert nrt == 5 and ns * ct >= 513 and (ns - 1) * ct < 513 and ct >= 2
+    # streams that alone fill a wave (16 x 5 row tiles > 76 clusters) are still
+    # cut into about four waves' worth of slices: 304 / 80 -> 4
+    assert mva.plan(16, 9, 64, 24320, 76)[1] == 4
     # H other than 64 and one query row
     assert mva.plan(1, 1, 1, 64, 76)[0] == 1
     assert mva.plan(2, 3, 16, 1000, 76)[0] == 1
