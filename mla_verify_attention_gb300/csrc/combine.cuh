@@ -40,12 +40,16 @@ __device__ __forceinline__ void wait_for_split_grid() {
 
 // kBatch 16: four blocks per SM (<= 128 registers), all rows of a 64-head,
 // 9-draft call in one wave; kBatch 8 and 4: 6 and 12 blocks per SM.
-template <int kBatch>
-__global__ void __launch_bounds__(128, kBatch == 16 ? 4 : (kBatch == 8 ? 6 : 12))
+// kGroups > 1 (calls with few rows and many slices, e.g. 8 heads): each of
+// kGroups groups of 128 threads merges every kGroups-th slice of the row, and
+// the groups' states are merged through shared memory at the end.
+template <int kBatch, int kGroups>
+__global__ void __launch_bounds__(128 * kGroups, kGroups > 1 ? 1 : (kBatch == 16 ? 4 : (kBatch == 8 ? 6 : 12)))
     combine_kernel(const CombineParams p) {
   wait_for_split_grid();
   const int row = blockIdx.x;
-  const int tid = threadIdx.x;
+  const int tid = threadIdx.x & 127;
+  const int grp = threadIdx.x >> 7;
   const int b = row / p.rows_per_stream;
   const int S = p.seq_lens[b];
   if (S < p.q || S > p.Smax) return;   // reported by the split kernel
@@ -59,12 +63,12 @@ __global__ void __launch_bounds__(128, kBatch == 16 ? 4 : (kBatch == 8 ? 6 : 12)
   // before any is used; batches are merged online (running max M).
   float M = -CUDART_INF_F, L = 0.f;
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-  for (int s0 = 0; s0 < ns; s0 += kBatch) {
+  for (int s0 = grp; s0 < ns; s0 += kBatch * kGroups) {
     float2 v[kBatch];
     float4 o[kBatch];
 #pragma unroll
     for (int e = 0; e < kBatch; ++e) {
-      const int s = s0 + e;
+      const int s = s0 + e * kGroups;
       if (s < ns) {
         v[e] = ml[static_cast<size_t>(s) * p.N];
         o[e] = src[s * step4];
@@ -90,6 +94,34 @@ __global__ void __launch_bounds__(128, kBatch == 16 ? 4 : (kBatch == 8 ? 6 : 12)
       acc.w += w * o[e].w;
     }
     M = Mb;
+  }
+  if (kGroups > 1) {
+    __shared__ float gm[kGroups], gl[kGroups];
+    __shared__ float4 gacc[kGroups][128];
+    if (tid == 0) {
+      gm[grp] = M;
+      gl[grp] = L;
+    }
+    gacc[grp][tid] = acc;
+    __syncthreads();
+    if (grp != 0) return;
+    M = -CUDART_INF_F;
+#pragma unroll
+    for (int g = 0; g < kGroups; ++g) M = gl[g] > 0.f ? fmaxf(M, gm[g]) : M;
+    L = 0.f;
+    acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (M != -CUDART_INF_F) {
+#pragma unroll
+      for (int g = 0; g < kGroups; ++g) {
+        const float w = gl[g] > 0.f ? ex2(gm[g] - M) : 0.f;
+        const float4 a = gacc[g][tid];
+        L += w * gl[g];
+        acc.x += w * a.x;
+        acc.y += w * a.y;
+        acc.z += w * a.z;
+        acc.w += w * a.w;
+      }
+    }
   }
   float4* dst = reinterpret_cast<float4*>(p.out + static_cast<size_t>(row) * 512) + tid;
   if (M == -CUDART_INF_F) {

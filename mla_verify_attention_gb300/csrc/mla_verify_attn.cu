@@ -472,8 +472,13 @@ int run(const Call& c) {
     // Slices per load batch: 16 while all rows fit one wave at four blocks per
     // SM, else 8 (more resident rows; batches are merged online).
     const int nb = ns <= 4 ? 4 : ((ns <= 8 || rows > 4LL * d->sms) ? 8 : 16);
-    if (cudaLaunchKernelEx(&cfg, nb == 4 ? mla::combine_kernel<4>
-                                 : (nb == 8 ? mla::combine_kernel<8> : mla::combine_kernel<16>),
+    // Few rows and many slices (e.g. 8 heads over a long stream): four groups
+    // of threads per row share the slices.
+    const bool grouped = ns > 16 && rows <= d->sms;
+    if (grouped) cfg.blockDim = dim3(4 * 128, 1, 1);
+    if (cudaLaunchKernelEx(&cfg, grouped ? mla::combine_kernel<16, 4>
+                                 : (nb == 4 ? mla::combine_kernel<4, 1>
+                                            : (nb == 8 ? mla::combine_kernel<8, 1> : mla::combine_kernel<16, 1>)),
                            c) != cudaSuccess) {
       cudaGetLastError();
       return MLA_ERR_LAUNCH;

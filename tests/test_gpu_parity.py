@@ -111,6 +111,14 @@ def test_edge_shapes(B, q, H, prefixes):
     check(case, *run_gpu(case))
 
 
+@pytest.mark.parametrize("nsplit", [17, 40])
+def test_few_rows_many_slices(nsplit):
+    # 72 rows (8 heads) over many slices: the merge shares a row's slices among
+    # four groups of threads.
+    case = custom_case(1, 9, 8, [5000], seed=61 + nsplit)
+    check(case, *run_gpu(case, nsplit=nsplit))
+
+
 def test_edge_shapes_split():
     case = custom_case(3, 5, 8, [10, 900, 2000], seed=77)
     check(case, *run_gpu(case, nsplit=4))
