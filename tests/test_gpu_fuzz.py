@@ -1,0 +1,83 @@
+"""Seeded random shapes through the C ABI against the fp64 oracle.
+
+Each case draws the stream count, draft count, head count, prefix lengths,
+tree shape, an optional forced slice count and an optional paged layout from
+one seeded generator, so that combinations the hand-written cases miss (ragged
+streams with the device plan, two-word masks with few heads, short slices with
+the merge, odd page sizes) are exercised at the same tolerances.
+"""
+import os
+
+import numpy as np
+import pytest
+
+import oracle
+from mla_verify_attention_gb300 import inputs as I
+
+pytestmark = pytest.mark.gpu
+
+TOL_OUT = 2e-3
+TOL_LSE = 1e-3
+N_CASES = 24
+
+
+def _draw(k):
+    rng = np.random.default_rng(20260 + k)
+    B = int(rng.integers(1, 7))
+    q = int(rng.choice([1, 2, 5, 9, 17, 33, 40]))
+    H = int(rng.choice([1, 8, 16, 64]))
+    prefixes = [int(x) for x in rng.integers(0, 3000, B)]
+    tree = "chain" if rng.random() < 0.25 else "random"
+    nsplit = int(rng.choice([0, 0, 2, 3, 9]))
+    page = int(rng.choice([0, 0, 0, 1, 16, 64, 192]))
+    return B, q, H, prefixes, tree, nsplit, page
+
+
+def _run(case, nsplit, page):
+    import torch
+    import mla_verify_attention_gb300 as mva
+    old = os.environ.get("MLA_VERIFY_NSPLIT")
+    if nsplit:
+        os.environ["MLA_VERIFY_NSPLIT"] = str(nsplit)
+    try:
+        def t(a, dt):
+            return torch.from_numpy(np.ascontiguousarray(a)).view(dt).cuda()
+        qn = t(case.q_nope.view(np.int16), torch.bfloat16)
+        qr = t(case.q_rope.view(np.int16), torch.bfloat16)
+        sl = t(case.seq_lens, torch.int32)
+        m = t(case.mask.view(np.int32), torch.int32)
+        if page:
+            pool, table = I.to_paged(case, page, seed=5)
+            out, lse = mva.verify_attn_paged(qn, qr, t(pool.view(np.int16), torch.bfloat16),
+                                             t(table, torch.int32), page, sl, m, float(case.scale))
+        else:
+            out, lse = mva.verify_attn(qn, qr, t(case.kv.view(np.int16), torch.bfloat16), sl, m,
+                                       float(case.scale))
+        torch.cuda.synchronize()
+        st = mva.last_device_error()
+    finally:
+        if nsplit:
+            if old is None:
+                os.environ.pop("MLA_VERIFY_NSPLIT", None)
+            else:
+                os.environ["MLA_VERIFY_NSPLIT"] = old
+    assert st == 0, mva.strerror(st)
+    return out.cpu().numpy().astype(np.float64), lse.cpu().numpy().astype(np.float64)
+
+
+@pytest.mark.parametrize("k", range(N_CASES))
+def test_random_shapes_match_oracle(k):
+    B, q, H, prefixes, tree, nsplit, page = _draw(k)
+    w = I.Workload("fuzz", B, q, 0, tree, 5, None, H=H, index=0)
+    case = I.make_case(w, seed=700 + k, prefixes=prefixes)
+    out, lse = _run(case, nsplit, page)
+    ref_out, ref_lse = oracle.case_reference(case)
+    o = out.reshape(ref_out.shape)
+    l = lse.reshape(ref_lse.shape)
+    empty = np.isneginf(ref_lse)
+    assert np.array_equal(np.isneginf(l), empty), (B, q, H, prefixes, nsplit, page)
+    assert np.all(o[empty] == 0.0)
+    assert np.isfinite(o).all()
+    d_out = np.abs(o - ref_out).max()
+    d_lse = np.abs(l[~empty] - ref_lse[~empty]).max() if (~empty).any() else 0.0
+    assert d_out <= TOL_OUT and d_lse <= TOL_LSE, (B, q, H, prefixes, nsplit, page, d_out, d_lse)
