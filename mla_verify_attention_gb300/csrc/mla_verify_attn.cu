@@ -28,7 +28,16 @@ constexpr int kMaxDevices = 64;
 // Measured on tree9/chain9 shapes: 2-tile slices beat longer ones while all
 // units fit one wave.
 constexpr int kMinTilesPerSlice = mla::kMinSliceTiles;
-constexpr int kTwoTermMaxKeys = 32768;        // streams up to this length send P as hi + lo
+// P precision.  Rounding P to one bf16 term (with the lazily kept row max)
+// put errors up to 4.8e-3 into outputs of streams of 4105..32760 keys, whose
+// few dominant keys carry much of each row's weight.  Caches of more than
+// kCorrectMaxKeys keys: streams up to kTwoTermMaxKeys send P as hi + lo.
+// Caches of up to kCorrectMaxKeys keys (the kCorrect kernel): streams up to
+// kTwoTermMaxKeysCorrected send hi + lo, longer ones one term plus the
+// correction of each row's dominant key.
+constexpr int kTwoTermMaxKeys = 32768;
+constexpr int kCorrectMaxKeys = 32768;
+constexpr int kTwoTermMaxKeysCorrected = 4096;
 constexpr size_t kSmemBytes = sizeof(mla::Smem) + 1024;   // + manual 1 KB alignment
 
 struct DeviceInfo {
@@ -75,21 +84,21 @@ int device_info(DeviceInfo** out) {
           q != cudaDriverEntryPointSuccess || fn == nullptr)
         d.status = MLA_ERR_UNSUPPORTED_DEVICE;
       d.encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
-      if (d.status == MLA_OK &&
-          (cudaFuncSetAttribute(mla::verify_split_kernel<false>,
-                                cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                static_cast<int>(kSmemBytes)) != cudaSuccess ||
-           cudaFuncSetAttribute(mla::verify_split_kernel<true>,
-                                cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                static_cast<int>(kSmemBytes)) != cudaSuccess))
-        d.status = MLA_ERR_LAUNCH;
+      using SplitFn = void (*)(CUtensorMap, CUtensorMap, CUtensorMap, CUtensorMap, CUtensorMap,
+                               CUtensorMap, mla::SplitParams);
+      const SplitFn fns[4] = {mla::verify_split_kernel<false, false>, mla::verify_split_kernel<true, false>,
+                              mla::verify_split_kernel<false, true>, mla::verify_split_kernel<true, true>};
+      for (const SplitFn fn : fns)
+        if (d.status == MLA_OK && cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                       static_cast<int>(kSmemBytes)) != cudaSuccess)
+          d.status = MLA_ERR_LAUNCH;
       if (d.status == MLA_OK) {
         cudaLaunchConfig_t cfg = {};
         cfg.gridDim = dim3(2 * sms, 1, 1);
         cfg.blockDim = dim3(mla::kThreads, 1, 1);
         cfg.dynamicSmemBytes = kSmemBytes;
         int n = 0;
-        if (cudaOccupancyMaxActiveClusters(&n, mla::verify_split_kernel<false>, &cfg) != cudaSuccess ||
+        if (cudaOccupancyMaxActiveClusters(&n, mla::verify_split_kernel<false, false>, &cfg) != cudaSuccess ||
             n < 1)
           n = sms / 2;
         d.max_clusters = n;
@@ -371,7 +380,11 @@ int run(const Call& c) {
                                                          plan_offset(B, q_len, H, ns))
                                 : nullptr;
   p.plan = plan_dev;
-  p.two_term_max_keys = kTwoTermMaxKeys;
+  const bool corrected = Smax <= kCorrectMaxKeys;
+  const int two_term_max_keys = corrected ? kTwoTermMaxKeysCorrected : kTwoTermMaxKeys;
+  p.two_term_max_keys = two_term_max_keys;
+  p.kv = static_cast<const uint8_t*>(kv);
+  p.kv_rows = paged ? c.pool_rows : static_cast<long long>(Smax);
   const char* stall = std::getenv("MLA_VERIFY_TEST_STALL");
   p.test_stall = (stall && stall[0] && stall[0] != '0') ? 1 : 0;
   p.scale_log2 = scale * 1.4426950408889634f;
@@ -408,7 +421,7 @@ int run(const Call& c) {
     pp.nsplit_max = ns;
     pp.min_chunk = kMinTilesPerSlice;
     pp.slots = d->max_clusters;
-    pp.two_term_max_keys = kTwoTermMaxKeys;
+    pp.two_term_max_keys = two_term_max_keys;
     const int ncand = ns < mla::kPlanMaxCandidates ? ns : mla::kPlanMaxCandidates;
     mla::plan_kernel<<<1, 32 * ncand, 0, stream>>>(pp);
     if (cudaGetLastError() != cudaSuccess) return MLA_ERR_LAUNCH;
@@ -433,8 +446,14 @@ int run(const Call& c) {
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = after_copy ? 1 : 0;
-    if (cudaLaunchKernelEx(&cfg, after_copy ? mla::verify_split_kernel<true> : mla::verify_split_kernel<false>,
-                           map_qn, map_qr, map_kvs0, map_kvs1, map_kvo, map_out, p) != cudaSuccess) {
+    using SplitFn = void (*)(CUtensorMap, CUtensorMap, CUtensorMap, CUtensorMap, CUtensorMap,
+                             CUtensorMap, mla::SplitParams);
+    const SplitFn fn = corrected ? (after_copy ? mla::verify_split_kernel<true, true>
+                                               : mla::verify_split_kernel<false, true>)
+                                 : (after_copy ? mla::verify_split_kernel<true, false>
+                                               : mla::verify_split_kernel<false, false>);
+    if (cudaLaunchKernelEx(&cfg, fn, map_qn, map_qr, map_kvs0, map_kvs1, map_kvo, map_out, p) !=
+        cudaSuccess) {
       cudaGetLastError();
       return MLA_ERR_LAUNCH;
     }

@@ -37,7 +37,12 @@
 // rounded to bf16 because V is bf16 in the cache.  With the lazily kept row
 // max even the dominant key's p carries that rounding, so streams up to
 // two_term_max_keys keys (where a few keys carry most of the weight) send P as
-// two bf16 terms hi + lo and the PV product is issued once per term.
+// two bf16 terms hi + lo and the PV product is issued once per term.  The
+// kCorrect instantiation (caches of up to 32768 keys) sends one term for the
+// longer of those streams and removes the dominant key's rounding instead:
+// the softmax threads keep, per row, the key with the largest score and the
+// error p - bf16(p) of its P (rescaled with O), and the O CTA adds error x
+// that key's value row to the accumulator before the epilogue.
 //
 // Units start in index order.  For 2..32 streams the index order is a list
 // schedule (ordered_slice), and the slice length may come from plan_kernel
@@ -88,6 +93,17 @@ constexpr int kOutBufs = 6;                      // staging blocks per helper ha
 static_assert(2 * kOutBufs * kOutBlock <= kRingBytes, "epilogue staging must fit the ring");
 constexpr int kRowThreads = 256;                 // two threads per row (one per 32-key half)
 constexpr uint32_t kQCols = 288;                 // Q in tensor memory: 576 bf16 = 288 cols
+// Dominant-key correction (kCorrect): a key is skipped when its P is below
+// 2^-kCorrKeepLog2 of its half's running sum, and a row's correction when its
+// error is not above 2^-kCorrSkipLog2 of the row sum; either way a skipped
+// term moves the output by at most 2^-13 of a value entry.
+constexpr float kCorrKeepLog2 = 4.0f;
+constexpr float kCorrSkipLog2 = 13.0f;
+// Per helper warp: 32 rows x 64 bytes of value rows, the transpose buffer of
+// the correction's coalesced loads, after the epilogue's staging blocks.
+constexpr int kCorrBufOffset = 2 * kOutBufs * kOutBlock;
+constexpr int kCorrWarpBytes = 32 * 64;
+static_assert(kCorrBufOffset + 8 * kCorrWarpBytes <= kRingBytes, "correction buffers must fit the ring");
 constexpr float kLazyRescale = 8.0f;             // log2 units: keep the max unless it grows by 2^8
 constexpr uint64_t kWaitNs = 2000000000ull;      // bounded waits: 2 s
 
@@ -121,6 +137,10 @@ struct SplitParams {
   // plan_kernel from the stream lengths (null: the host's values hold).  nsplit
   // above stays the host's (grid, workspace, partials or direct output).
   const int* plan;
+  // The cache the tensor maps describe, for the dominant-key correction's
+  // row reads: [streams][kv_rows][576] bf16 (paged: one stream of pool rows).
+  const uint8_t* kv;
+  long long kv_rows;
 };
 
 struct __align__(1024) Smem {
@@ -128,6 +148,9 @@ struct __align__(1024) Smem {
   float2 ml[kRows];
   float xmax[2][kRows];      // S CTA: per-half partial row max of the current tile
   float xl[kRows];           // S CTA: second half's running sum, combined at the end
+  float2 xbest[kRows];       // S CTA: second half's {largest score, its P error}
+  int xkey[kRows];           //   and that key (kCorrect)
+  float2 corr[kRows];        // O CTA: {P error, key} of the row's dominant key (kCorrect)
   uint64_t kfull[2][kKSlots], kempty[2][kKSlots];   // [part][slot]
   uint64_t qfull, qready;
   uint64_t sfull[2], sempty[2];
@@ -411,7 +434,8 @@ __device__ __forceinline__ void s_mma(Smem& sm, const Unit& u, const SplitParams
 // tile, the second keys 32..63.  The two halves agree on the row max through
 // shared memory once per tile; each keeps its own part of the running sum.
 // kTwoTerm: P goes out as two bf16 terms hi + lo (short streams).
-template <bool kTwoTerm>
+// kCorrect: one term, plus the dominant key's rounding error for the O CTA.
+template <bool kTwoTerm, bool kCorrect>
 __device__ __forceinline__ void s_softmax(Smem& sm, const Unit& u, const SplitParams& p,
                                           uint32_t tmem, int wq, int half, int lane) {
   const int r = wq * 32 + lane;                     // row of the unit == tensor-memory lane
@@ -469,6 +493,11 @@ __device__ __forceinline__ void s_softmax(Smem& sm, const Unit& u, const SplitPa
   float l = 0.f;                  // this half's running sum of P
   bool copy_failed = false;       // set by the copy-issuing thread only
   bool finished = true;
+  // kCorrect: this half's largest log2-scaled score so far, its key and the
+  // rounding error p - bf16(p) of the P staged for it (in O's current scale).
+  float best_x = -CUDART_INF_F;
+  float best_e = 0.f;
+  int best_key = 0;
 
   // Stage P (and the row sums) for 8 keys at a time into exchange buffer `xb`
   // [alpha | flags | P hi | P lo] with exponent offset msub; returns the sum.
@@ -510,6 +539,7 @@ __device__ __forceinline__ void s_softmax(Smem& sm, const Unit& u, const SplitPa
     const bool got = warp_wait(sm, smem_u32(&sm.sfull[buf]), (j >> 1) & 1, p, 7);
     uint32_t sr[32];
     float mh = -CUDART_INF_F;   // this half's tile max (log2-scaled)
+    float mraw = -CUDART_INF_F; // the same before the scale (kCorrect)
     if (got) {
       tc_fence_after();
       MLA_TMEM_LD_32x32b_X32(tmem + lane_base + kQCols + 64 * buf + 32 * half, sr);
@@ -543,7 +573,8 @@ __device__ __forceinline__ void s_softmax(Smem& sm, const Unit& u, const SplitPa
       for (int k = 0; k < 4; ++k) mx[k] = __uint_as_float(sr[k]);
 #pragma unroll
       for (int c = 4; c < 32; ++c) mx[c & 3] = fmaxf(mx[c & 3], __uint_as_float(sr[c]));
-      mh = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * a_eff;
+      mraw = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
+      mh = mraw * a_eff;
     }
     // Lazy rescale: P may exceed 1 by up to 2^kLazyRescale; O and l only get
     // rescaled (here and in the O CTA) when the max grows beyond that.  Each
@@ -579,6 +610,7 @@ __device__ __forceinline__ void s_softmax(Smem& sm, const Unit& u, const SplitPa
         flag = (m_used != -CUDART_INF_F);  // an all-zero O row needs no rescale
         m_used = mt;
         l *= alpha;
+        if (kCorrect) best_e *= alpha;
       }
       lsum = stage_p(sr, xb, m_used == -CUDART_INF_F ? 0.f : m_used);
       if (half == 0) {
@@ -600,14 +632,50 @@ __device__ __forceinline__ void s_softmax(Smem& sm, const Unit& u, const SplitPa
         copy_failed = true;
       }
     }
+    if (kCorrect && mh > best_x) {
+      // A new largest score of this half (after the copy is on its way):
+      // recompute its P exactly as staged (same fused multiply-add and exp2).
+      // Kept, with its bf16 rounding error, when P is not below 2^-4 of the
+      // running sum (this tile included): a smaller share can only shrink.
+      // (A test against the exponent bits of l instead of the exp2 kept keys
+      // down to l / 32, ran the search below more often and was slower.)
+      const float msub = m_used == -CUDART_INF_F ? 0.f : m_used;
+      const float pv = ex2(fmaf(mraw, a_eff, -msub));
+      best_x = mh;
+      if (pv >= l * exp2f(-kCorrKeepLog2)) {
+        int cb = 0;
+#pragma unroll
+        for (int c = 31; c >= 0; --c)
+          if (__uint_as_float(sr[c]) == mraw) cb = c;
+        best_e = pv - bf16lo_to_f32(pack_bf16x2(pv, pv));
+        best_key = u.k0 + j * kKeys + 32 * half + cb;
+      }
+    }
   }
   if (half == 0 && r == 0) bulk_wait_read<0>();
   if (!finished) return;
-  if (half == 1) sm.xl[r] = l;
+  if (half == 1) {
+    sm.xl[r] = l;
+    if (kCorrect) {
+      sm.xbest[r] = make_float2(best_x, best_e);
+      sm.xkey[r] = best_key;
+    }
+  }
   if (named_bar_red_or(kSoftmaxBar, kRowThreads, copy_failed)) return;
-  if (half == 0)
+  if (half == 0) {
+    const uint32_t mlfull_remote = mapa_shared(smem_u32(&sm.mlfull), peer);
     st_async_v2(mapa_shared(smem_u32(&sm.ml[r]), peer), __float_as_uint(m_used),
-                __float_as_uint(l + sm.xl[r]), mapa_shared(smem_u32(&sm.mlfull), peer));
+                __float_as_uint(l + sm.xl[r]), mlfull_remote);
+    if (kCorrect) {
+      const float2 other = sm.xbest[r];
+      if (other.x > best_x) {
+        best_e = other.y;
+        best_key = sm.xkey[r];
+      }
+      st_async_v2(mapa_shared(smem_u32(&sm.corr[r]), peer), __float_as_uint(best_e),
+                  static_cast<uint32_t>(best_key), mlfull_remote);
+    }
+  }
 }
 
 // ============================================================ O CTA roles
@@ -721,11 +789,35 @@ __device__ __forceinline__ void o_mma(Smem& sm, const Unit& u, const SplitParams
   __syncwarp();
 }
 
+// Cache row of key `key` of the unit's stream (576 bf16).
+__device__ __forceinline__ const uint8_t* cache_row(const SplitParams& p, const Unit& u, int key) {
+  const int2 o = p.block_table != nullptr ? tile_origin<true>(p, u, key) : tile_origin<false>(p, u, key);
+  return p.kv + (static_cast<size_t>(o.y) * static_cast<size_t>(p.kv_rows) + static_cast<size_t>(o.x)) *
+                    static_cast<size_t>((kDl + kDr) * 2);
+}
+
+// 8 value columns (one 16-byte load of bf16) times e, added to 8 fp32 bit patterns.
+__device__ __forceinline__ void add_scaled_bf16x8(uint32_t* v, const uint4& x, float e) {
+  const uint32_t w[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    v[2 * k] = __float_as_uint(fmaf(e, __uint_as_float(w[k] << 16), __uint_as_float(v[2 * k])));
+    v[2 * k + 1] =
+        __float_as_uint(fmaf(e, __uint_as_float(w[k] & 0xFFFF0000u), __uint_as_float(v[2 * k + 1])));
+  }
+}
+
 // Eight helper warps: warp 4+w and warp 8+w own tensor-memory lanes
 // 32w..32w+31 (one output row per lane) and split the 512 accumulator columns.
+// kCorrect (with `corr`): the epilogue adds the dominant key's P error times
+// its value row to each row.  The value rows are read one 32-column block
+// ahead, each warp's 32 rows together (four lanes per row, eight rows per
+// load instruction, instead of 32 rows per instruction), and handed to the
+// rows' threads through a per-warp shared-memory buffer.
+template <bool kCorrect>
 __device__ __forceinline__ void o_helpers(Smem& sm, const Unit& u, const SplitParams& p,
                                           const CUtensorMap* map_out, uint32_t tmem, int wq,
-                                          int half, int lane) {
+                                          int half, int lane, bool corr) {
   const int r = wq * 32 + lane;
   const uint32_t lane_base = static_cast<uint32_t>(wq * 32) << 16;
   const uint32_t col0 = 256u * half;
@@ -783,8 +875,41 @@ __device__ __forceinline__ void o_helpers(Smem& sm, const Unit& u, const SplitPa
   // The staging below uses named barriers: all 128 threads of a half decide
   // together whether the results are complete.
   const uint32_t bar = kEpilogueBar + static_cast<uint32_t>(half);
-  const bool ready = !failed && warp_wait(sm, smem_u32(&sm.odone), 0, p, 15) &&
-                     warp_wait<true>(sm, smem_u32(&sm.mlfull), 0, p, 16);
+  bool ready;
+  // kCorrect: this row's P error; rows of the warp that need a correction;
+  // this lane's load slots: rows 8i + lane/4 (i = 0..3), 16 bytes at lane%4.
+  float ce = 0.f;
+  uint32_t need = 0u;
+  const uint8_t* lrow[4] = {nullptr, nullptr, nullptr, nullptr};
+  uint4 lx[4];
+  if (kCorrect) {
+    // (Waiting for the softmax results before the last PV, to start these
+    // loads earlier, made the 33-draft, 16384-key call 2.2 us slower.)
+    ready = !failed && warp_wait(sm, smem_u32(&sm.odone), 0, p, 15) &&
+            warp_wait<true>(sm, smem_u32(&sm.mlfull), 0, p, 16);
+    const uint8_t* vrow = nullptr;
+    if (ready && corr) {
+      const float2 cr = sm.corr[r];
+      const float lrow_sum = sm.ml[r].y;
+      if (r < u.valid_rows && fabsf(cr.x) > lrow_sum * exp2f(-kCorrSkipLog2)) {
+        ce = cr.x;
+        vrow = cache_row(p, u, static_cast<int>(__float_as_uint(cr.y))) + col0 * 2;
+      }
+    }
+    need = __ballot_sync(0xFFFFFFFFu, ce != 0.f);
+    if (need) {
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int rr = 8 * i + (lane >> 2);
+        const uint64_t a = __shfl_sync(0xFFFFFFFFu, reinterpret_cast<uint64_t>(vrow), rr);
+        lrow[i] = reinterpret_cast<const uint8_t*>(a) + 16 * (lane & 3);
+        if ((need >> rr) & 1u) lx[i] = *reinterpret_cast<const uint4*>(lrow[i]);
+      }
+    }
+  } else {
+    ready = !failed && warp_wait(sm, smem_u32(&sm.odone), 0, p, 15) &&
+            warp_wait<true>(sm, smem_u32(&sm.mlfull), 0, p, 16);
+  }
   if (named_bar_red_or(bar, kRows, !ready)) return;
   tc_fence_after();
   const float2 ml = sm.ml[r];
@@ -817,6 +942,34 @@ __device__ __forceinline__ void o_helpers(Smem& sm, const Unit& u, const SplitPa
       if (issuer) bulk_wait_read<kOutBufs - 2>();
       named_bar_sync(bar, kRows);
     }
+    if (kCorrect && need) {
+      // Block cc of the warp's value rows: loaded lanes -> buffer (row-major,
+      // 64 bytes a row, 16-byte units XOR-swizzled by (row >> 1) & 3, so that
+      // neither side has bank conflicts) -> each row's own thread.
+      uint8_t* wbuf = sm.ring + kCorrBufOffset + (half * 4 + wq) * kCorrWarpBytes;
+      __syncwarp();
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int rr = 8 * i + (lane >> 2);
+        if ((need >> rr) & 1u)
+          *reinterpret_cast<uint4*>(wbuf + rr * 64 + 16 * ((lane & 3) ^ ((rr >> 1) & 3))) = lx[i];
+      }
+      __syncwarp();
+      uint4 c[4];
+#pragma unroll
+      for (int k = 0; k < 4; ++k)
+        c[k] = *reinterpret_cast<const uint4*>(wbuf + lane * 64 + 16 * (k ^ ((lane >> 1) & 3)));
+      if (cc + 1 < 8) {
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+          if ((need >> (8 * i + (lane >> 2))) & 1u)
+            lx[i] = *reinterpret_cast<const uint4*>(lrow[i] + 64 * (cc + 1));
+      }
+      if (ce != 0.f) {
+#pragma unroll
+        for (int k = 0; k < 4; ++k) add_scaled_bf16x8(v + 8 * k, c[k], ce);
+      }
+    }
 #pragma unroll
     for (int e = 0; e < 8; ++e)
       *reinterpret_cast<float4*>(blk + r * 128 + ((e ^ (r & 7)) << 4)) =
@@ -840,8 +993,10 @@ __device__ __forceinline__ void o_helpers(Smem& sm, const Unit& u, const SplitPa
 // kAfterCopy: launched as a programmatic dependent of the grid that copied a
 // paged cache into a contiguous one; the cache loads first wait for that grid
 // (a separate instantiation: the wait instruction in the kernel cost ~0.7 us
-// per call even when not executed).
-template <bool kAfterCopy>
+// per call even when not executed).  kCorrect: units that send one P term also
+// remove their dominant keys' rounding (a separate instantiation too, so that
+// the kernel for longer caches carries none of its code).
+template <bool kAfterCopy, bool kCorrect>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     verify_split_kernel(const __grid_constant__ CUtensorMap map_qn,
                         const __grid_constant__ CUtensorMap map_qr,
@@ -857,6 +1012,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   const int lane = tid & 31;
   const uint32_t role = cluster_ctarank();   // 0: scores + softmax, 1: PV accumulator
   const Unit u = decode_unit(p);
+  const bool corr = kCorrect && !u.two_term;   // one-term P plus the dominant-key correction
   // The slice merge is launched as a programmatic dependent of this grid; it
   // may be scheduled now and waits for this grid's completion itself.
   if (tid == 0) grid_launch_dependents();
@@ -901,7 +1057,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       // P buffers 0 and 1 expect tiles 0 and 1; m/l expect one pair per row.
       mbar_arrive_expect_tx(smem_u32(&sm.pfull[0]), p_tile_bytes(u));
       if (u.ntiles > 1) mbar_arrive_expect_tx(smem_u32(&sm.pfull[1]), p_tile_bytes(u));
-      mbar_arrive_expect_tx(smem_u32(&sm.mlfull), kRows * 8);
+      mbar_arrive_expect_tx(smem_u32(&sm.mlfull), kRows * (corr ? 16 : 8));
     }
     fence_mbarrier_init_cluster();
     fence_proxy_async_smem();   // the initialised barriers, before TMA completes on them
@@ -947,9 +1103,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         __syncwarp();
       } else if (warp >= 4) {
         if (u.two_term)
-          s_softmax<true>(sm, u, p, tmem, warp & 3, (warp - 4) >> 2, lane);  // half = warp / 4 - 1
+          s_softmax<true, false>(sm, u, p, tmem, warp & 3, (warp - 4) >> 2, lane);  // half = warp / 4 - 1
         else
-          s_softmax<false>(sm, u, p, tmem, warp & 3, (warp - 4) >> 2, lane);
+          s_softmax<false, kCorrect>(sm, u, p, tmem, warp & 3, (warp - 4) >> 2, lane);
       }
     } else {
       if (warp == 0 && lane == 0) {
@@ -964,7 +1120,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         mbar_wait(smem_u32(&sm.drain), 0, kWaitNs);
         __syncwarp();
       } else if (warp >= 4) {
-        o_helpers(sm, u, p, &map_out, tmem, warp & 3, (warp - 4) >> 2, lane);
+        o_helpers<kCorrect>(sm, u, p, &map_out, tmem, warp & 3, (warp - 4) >> 2, lane, corr);
       }
     }
   }

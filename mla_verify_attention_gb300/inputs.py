@@ -280,6 +280,19 @@ def to_paged(case: "Case", page_size: int, seed: int, extra_pages: int = 3):
     return pool, np.ascontiguousarray(table)
 
 
+def scale_key_rope(case: "Case", b: int, key: int, factor: float) -> None:
+    """Scale the rope part (the last Dr values) of one cache row in place.
+
+    The key's score grows in every row whose q_pe agrees with its k_pe, so it
+    dominates those rows' softmax while its value row (the latent part) keeps
+    the distribution of the others: inputs on which a rounded weight of the
+    dominant key shows in the output.
+    """
+    row = bf16_bits_to_f32(case.kv[b, key]).copy()
+    row[-case.kv.shape[2] + 512:] *= np.float32(factor)
+    case.kv[b, key] = f32_to_bf16_bits(row)
+
+
 def make_case(w: Workload, seed: int | None = None, pad: str = "nan",
               smax_align: int = 64, prefixes=None) -> Case:
     """Materialise a workload.

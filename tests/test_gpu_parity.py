@@ -166,11 +166,29 @@ def test_bad_stream_length_is_reported(B):
 def test_precision_across_stream_lengths(S, seed):
     # Inputs on which bf16 P in one term missed the tolerance (4.8e-3 at 2100
     # keys, 2.4e-3 at 12000): with a lazily updated row max, even the dominant
-    # key's weight carries the bf16 rounding error.  Streams up to 32768 keys
-    # send P as two terms; at 32800 one term stays well inside (~6e-4).
+    # key's weight carries the bf16 rounding error.  In these caches (up to
+    # 32768 keys) streams up to 4096 keys send P as two terms and longer ones
+    # one term plus the dominant key's correction; at 32800 keys (a larger
+    # cache) one term stays well inside (~6e-4).
     w = I.Workload("custom", 1, 9, 0, "random", 5, None, H=64, index=0)
     case = I.make_case(w, seed=seed, prefixes=[S - 9])
     check(case, *run_gpu(case))
+
+
+# A planted key (its rope part scaled) dominates about half of the rows.  With
+# the lazily kept row max its P is rounded to bf16; sent as one term without
+# the dominant-key correction, these inputs put 2.2e-3 .. 3.8e-3 into the
+# output (fp64 emulation of that path).  Streams of more than 4096 keys in
+# caches of up to 32768 keys send one term and correct the dominant key.
+@pytest.mark.parametrize("S,key,factor,seed,q,nsplit", [
+    (8009, 7000, 10.0, 1, 9, None), (8009, 7000, 10.0, 1, 9, 1),
+    (6009, 5100, 8.0, 2, 9, None), (10033, 9000, 8.0, 4, 33, 3)])
+def test_dominant_key_correction(S, key, factor, seed, q, nsplit):
+    case = custom_case(1, q, 64, [S - q], seed, max_depth=8 if q > 9 else 5,
+                       max_children=4 if q > 9 else None)
+    I.scale_key_rope(case, 0, key, factor)
+    d_out, _ = check(case, *run_gpu(case, nsplit=nsplit))
+    assert d_out <= 1.2e-3, d_out
 
 
 def test_empty_rows_are_zero_and_minus_inf():

@@ -66,6 +66,21 @@ def test_paged_matches_oracle(B, q, H, prefixes, page_size):
     check(case, out, lse)
 
 
+@pytest.mark.parametrize("page_size", [64, 16])
+def test_paged_dominant_key_correction(page_size):
+    # One term plus the dominant key's correction, whose value row is read
+    # through the block table (64-key pages) or from the copy (16-row pages).
+    # Without the correction these inputs are off by 3.8e-3.
+    w = I.Workload("custom", 1, 9, 0, "random", 5, None, H=64, index=0)
+    case = I.make_case(w, seed=2, prefixes=[6000])
+    I.scale_key_rope(case, 0, 5100, 8.0)
+    out, lse = run_paged(case, page_size)
+    check(case, out, lse)
+    ref_out, _ = oracle.case_reference(case)
+    d = np.abs(out.cpu().numpy().astype(np.float64).reshape(ref_out.shape) - ref_out).max()
+    assert d <= 1.2e-3, d
+
+
 def test_paged_equals_contiguous_bitwise():
     import torch
     import mla_verify_attention_gb300 as mva
