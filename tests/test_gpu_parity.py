@@ -191,6 +191,23 @@ def test_dominant_key_correction(S, key, factor, seed, q, nsplit):
     assert d_out <= 1.2e-3, d_out
 
 
+# scale <= 0 takes the kernel's other softmax path (scores scaled before the
+# row max instead of inside the exp2); 700 keys send P in two terms, 6000 keys
+# (a cache of <= 32768) one term plus the dominant-key correction.
+@pytest.mark.parametrize("S,scale", [(700, -1.0 / np.sqrt(192.0)), (6000, -1.0 / np.sqrt(192.0)),
+                                     (6000, 0.0), (700, 0.0)])
+def test_non_positive_scale(S, scale):
+    case = custom_case(1, 9, 64, [S - 9], seed=404 + S)
+    case.scale = np.float32(scale)
+    out, lse = run_gpu(case)
+    check(case, out, lse)
+    if scale == 0.0:
+        # every visible key has weight 1: lse = ln(number of visible keys)
+        P = S - 9
+        seen = np.array([P + bin(int(case.mask[0, i, 0]) & 0x1FF).count("1") for i in range(9)])
+        np.testing.assert_allclose(lse.reshape(9, 64), np.log(seen)[:, None].repeat(64, 1), atol=1e-5)
+
+
 def test_empty_rows_are_zero_and_minus_inf():
     case = custom_case(1, 4, 64, [0], seed=9, tree="chain")
     case.mask[0, 0, 0] = 0          # draft 0 sees nothing at all
