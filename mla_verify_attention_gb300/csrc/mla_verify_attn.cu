@@ -86,8 +86,12 @@ int device_info(DeviceInfo** out) {
       d.encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
       using SplitFn = void (*)(CUtensorMap, CUtensorMap, CUtensorMap, CUtensorMap, CUtensorMap,
                                CUtensorMap, mla::SplitParams);
-      const SplitFn fns[4] = {mla::verify_split_kernel<false, false>, mla::verify_split_kernel<true, false>,
-                              mla::verify_split_kernel<false, true>, mla::verify_split_kernel<true, true>};
+      const SplitFn fns[6] = {mla::verify_split_kernel<mla::kDepNone, false>,
+                              mla::verify_split_kernel<mla::kDepCopy, false>,
+                              mla::verify_split_kernel<mla::kDepPlan, false>,
+                              mla::verify_split_kernel<mla::kDepNone, true>,
+                              mla::verify_split_kernel<mla::kDepCopy, true>,
+                              mla::verify_split_kernel<mla::kDepPlan, true>};
       for (const SplitFn fn : fns)
         if (d.status == MLA_OK && cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                                        static_cast<int>(kSmemBytes)) != cudaSuccess)
@@ -98,7 +102,7 @@ int device_info(DeviceInfo** out) {
         cfg.blockDim = dim3(mla::kThreads, 1, 1);
         cfg.dynamicSmemBytes = kSmemBytes;
         int n = 0;
-        if (cudaOccupancyMaxActiveClusters(&n, mla::verify_split_kernel<false, false>, &cfg) != cudaSuccess ||
+        if (cudaOccupancyMaxActiveClusters(&n, mla::verify_split_kernel<mla::kDepNone, false>, &cfg) != cudaSuccess ||
             n < 1)
           n = sms / 2;
         d.max_clusters = n;
@@ -427,10 +431,12 @@ int run(const Call& c) {
     if (cudaGetLastError() != cudaSuccess) return MLA_ERR_LAUNCH;
   }
   const bool timing = g_timing_before != nullptr;
-  // After the cache copy the split kernel is its programmatic dependent
-  // (prologue overlapped, cache loads wait for the copy to complete); after
-  // the planner it starts in plain stream order (its units follow the plan).
-  const bool after_copy = copy && !timing && !planned;
+  // The split kernel is a programmatic dependent of the grid before it: of
+  // the cache copy (prologue overlapped, cache loads wait for the copy), or of
+  // the planner (launch overlapped, every thread waits for the plan).  Not
+  // while the timing events are recorded between the launches.
+  const int dep = timing ? mla::kDepNone
+                         : (planned ? mla::kDepPlan : (copy ? mla::kDepCopy : mla::kDepNone));
   if (timing && cudaEventRecord(g_timing_before, stream) != cudaSuccess) {
     cudaGetLastError();
     return MLA_ERR_LAUNCH;
@@ -445,13 +451,16 @@ int run(const Call& c) {
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = after_copy ? 1 : 0;
+    cfg.numAttrs = dep != mla::kDepNone ? 1 : 0;
     using SplitFn = void (*)(CUtensorMap, CUtensorMap, CUtensorMap, CUtensorMap, CUtensorMap,
                              CUtensorMap, mla::SplitParams);
-    const SplitFn fn = corrected ? (after_copy ? mla::verify_split_kernel<true, true>
-                                               : mla::verify_split_kernel<false, true>)
-                                 : (after_copy ? mla::verify_split_kernel<true, false>
-                                               : mla::verify_split_kernel<false, false>);
+    const SplitFn fns[2][3] = {{mla::verify_split_kernel<mla::kDepNone, false>,
+                                mla::verify_split_kernel<mla::kDepCopy, false>,
+                                mla::verify_split_kernel<mla::kDepPlan, false>},
+                               {mla::verify_split_kernel<mla::kDepNone, true>,
+                                mla::verify_split_kernel<mla::kDepCopy, true>,
+                                mla::verify_split_kernel<mla::kDepPlan, true>}};
+    const SplitFn fn = fns[corrected ? 1 : 0][dep];
     if (cudaLaunchKernelEx(&cfg, fn, map_qn, map_qr, map_kvs0, map_kvs1, map_kvo, map_out, p) !=
         cudaSuccess) {
       cudaGetLastError();

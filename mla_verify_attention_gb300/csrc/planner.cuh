@@ -18,6 +18,8 @@
 #pragma once
 #include <cstdint>
 
+#include "ptx.cuh"
+
 namespace mla {
 
 constexpr int kPlanMaxCandidates = 12;   // the largest counts up to nsplit_max
@@ -45,6 +47,9 @@ __device__ __forceinline__ unsigned plan_time(float us) { return static_cast<uns
 __global__ void __launch_bounds__(32 * kPlanMaxCandidates, 1) plan_kernel(const PlanParams p) {
   __shared__ unsigned cost[kPlanMaxCandidates];
   __shared__ int chunk_of[kPlanMaxCandidates];
+  // The split kernel is this grid's programmatic dependent: it may be
+  // scheduled now and waits for this grid's completion before reading the plan.
+  if (threadIdx.x == 0) grid_launch_dependents();
   const int lane = threadIdx.x & 31;
   const int warp = threadIdx.x >> 5;
   const int ncand = blockDim.x >> 5;

@@ -173,6 +173,8 @@ struct Unit {
 
 // Streams up to which slices are started longest first (one lane per stream).
 constexpr int kOrderedStreams = 32;
+// How the split kernel follows the preceding grid (template parameter kDep).
+constexpr int kDepNone = 0, kDepCopy = 1, kDepPlan = 2;
 constexpr int kMinSliceTiles = 2;   // shortest slice: a unit's fixed cost needs a few tiles
 
 // Slice (stream b, index sp, stream length S_b) of the t-th slice in start
@@ -990,13 +992,17 @@ __device__ __forceinline__ void o_helpers(Smem& sm, const Unit& u, const SplitPa
 
 // ============================================================ kernel
 
-// kAfterCopy: launched as a programmatic dependent of the grid that copied a
-// paged cache into a contiguous one; the cache loads first wait for that grid
-// (a separate instantiation: the wait instruction in the kernel cost ~0.7 us
-// per call even when not executed).  kCorrect: units that send one P term also
+// kDep: how the kernel follows the grid before it in the stream.
+//   kDepNone: plain stream order.
+//   kDepCopy: programmatic dependent of the grid that copied a paged cache into
+//     a contiguous one; only the cache loads wait for that grid.
+//   kDepPlan: programmatic dependent of plan_kernel; every thread waits for the
+//     plan before decoding its unit (its launch overlaps the planner's run).
+// (Separate instantiations: the wait instruction in the kernel cost ~0.7 us per
+// call even when not executed.)  kCorrect: units that send one P term also
 // remove their dominant keys' rounding (a separate instantiation too, so that
 // the kernel for longer caches carries none of its code).
-template <bool kAfterCopy, bool kCorrect>
+template <int kDep, bool kCorrect>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     verify_split_kernel(const __grid_constant__ CUtensorMap map_qn,
                         const __grid_constant__ CUtensorMap map_qr,
@@ -1007,6 +1013,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   extern __shared__ uint8_t smem_raw[];
   Smem& sm = *reinterpret_cast<Smem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                       ~static_cast<uintptr_t>(1023));
+  constexpr bool kAfterCopy = kDep == kDepCopy;
+  if (kDep == kDepPlan) grid_dependency_wait();   // the plan is the preceding grid's output
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
   const int lane = tid & 31;
