@@ -188,8 +188,9 @@ const char* mla_verify_attn_strerror(int status);
  * once (pass <= 0 to query the current device).  Honours the environment
  * variable MLA_VERIFY_NSPLIT (a positive integer forces the slice count, for
  * testing the split path on small inputs).  For 2 to 32 streams (count not
- * forced) this is the largest plan: the call's first kernel may choose fewer
- * slices from the device's seq_lens, and the slices then start longest first.
+ * forced) this is the largest plan: a one-block planning kernel of the call
+ * may choose fewer slices from the device's seq_lens, and the slices then
+ * start longest first.
  * Returns MLA_OK or a status.
  */
 int mla_verify_attn_plan(int B, int q_len, int H, int Smax, int max_clusters, int* n_row_tiles,
