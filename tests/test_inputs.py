@@ -76,3 +76,15 @@ def test_workload_shapes():
     assert r.kv.shape[1] % 64 == 0 and r.kv.shape[1] >= r.seq_lens.max()
     assert r.seq_lens.min() >= 1024 + 9
     assert float(c.scale) == float(np.float32(1 / np.sqrt(192)))
+
+
+def test_scale_key_rope_changes_only_that_rope_part():
+    w = I.Workload("t", 1, 9, 0, "random", 5, None, H=4, index=0)
+    case = I.make_case(w, seed=3, prefixes=[200])
+    before = case.kv.copy()
+    I.scale_key_rope(case, 0, 150, 8.0)
+    changed = np.argwhere(case.kv != before)
+    assert set(changed[:, 1]) == {150} and changed[:, 2].min() >= 512
+    old = I.bf16_bits_to_f32(before[0, 150, 512:])
+    new = I.bf16_bits_to_f32(case.kv[0, 150, 512:])
+    np.testing.assert_array_equal(new, old * np.float32(8.0))   # a power of two: exact in bf16
