@@ -4,7 +4,9 @@ Each case draws the stream count, draft count, head count, prefix lengths,
 tree shape, an optional forced slice count and an optional paged layout from
 one seeded generator, so that combinations the hand-written cases miss (ragged
 streams with the device plan, two-word masks with few heads, short slices with
-the merge, odd page sizes) are exercised at the same tolerances.
+the merge, odd page sizes) are exercised at the same tolerances.  A second set
+draws long streams (log-uniform up to 40000 keys): P in one term plus the
+dominant-key correction, in two terms, and caches of more than 32768 keys.
 """
 import os
 
@@ -77,6 +79,39 @@ def test_random_shapes_match_oracle(k):
     empty = np.isneginf(ref_lse)
     assert np.array_equal(np.isneginf(l), empty), (B, q, H, prefixes, nsplit, page)
     assert np.all(o[empty] == 0.0)
+    assert np.isfinite(o).all()
+    d_out = np.abs(o - ref_out).max()
+    d_lse = np.abs(l[~empty] - ref_lse[~empty]).max() if (~empty).any() else 0.0
+    assert d_out <= TOL_OUT and d_lse <= TOL_LSE, (B, q, H, prefixes, nsplit, page, d_out, d_lse)
+
+
+# (seed index) of long-stream cases: nine in caches of <= 32768 keys, three in
+# larger ones; drawn as below, kept where the oracle finishes in seconds.
+LONG_CASES = [0, 1, 2, 4, 5, 6, 9, 10, 12, 36, 62, 74]
+
+
+def _draw_long(k):
+    rng = np.random.default_rng(91000 + k)
+    B = int(rng.integers(1, 5))
+    q = int(rng.choice([1, 5, 9, 17, 33]))
+    H = int(rng.choice([8, 16, 64]))
+    prefixes = [int(np.exp(rng.uniform(np.log(500), np.log(40000)))) for _ in range(B)]
+    nsplit = int(rng.choice([0, 0, 0, 3]))
+    page = int(rng.choice([0, 0, 64, 16]))
+    return B, q, H, prefixes, nsplit, page
+
+
+@pytest.mark.parametrize("k", LONG_CASES)
+def test_long_streams_match_oracle(k):
+    B, q, H, prefixes, nsplit, page = _draw_long(k)
+    w = I.Workload("fuzzbig", B, q, 0, "random", 5, None, H=H, index=0)
+    case = I.make_case(w, seed=9100 + k, prefixes=prefixes)
+    out, lse = _run(case, nsplit, page)
+    ref_out, ref_lse = oracle.case_reference(case)
+    o = out.reshape(ref_out.shape)
+    l = lse.reshape(ref_lse.shape)
+    empty = np.isneginf(ref_lse)
+    assert np.array_equal(np.isneginf(l), empty)
     assert np.isfinite(o).all()
     d_out = np.abs(o - ref_out).max()
     d_lse = np.abs(l[~empty] - ref_lse[~empty]).max() if (~empty).any() else 0.0
