@@ -105,6 +105,8 @@ def test_forced_split_and_combine(nsplit):
     (1, 9, 16, [500]),          # fewer heads (row tile spans drafts)
     (3, 5, 8, [10, 200, 65]),   # ragged, tiny row count
     (1, 2, 128, [90]),          # more heads than a row tile
+    (1, 64, 16, [6000]),        # widest draft count, one P term + dominant-key correction
+    (2, 64, 8, [5000, 40000]),  # same, cache > 32768 keys: two terms, then one term
 ])
 def test_edge_shapes(B, q, H, prefixes):
     case = custom_case(B, q, H, prefixes, seed=7 + q + H + sum(prefixes))
