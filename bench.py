@@ -55,6 +55,10 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget-s", type=float, default=20.0)
     ap.add_argument("--e2e-steps", type=int, default=20)
+    ap.add_argument("--configs", choices=["all", "none"], default="all",
+                    help="also time every workload (the per-config table in the JSON line)")
+    ap.add_argument("--config-windows", type=int, default=5,
+                    help="windows of back-to-back calls per workload in that table (median)")
     ap.add_argument("--page-size", type=int, default=0,
                     help="time the paged-cache entry point with pages of this many keys "
                          "(a multiple of 64, pages in seeded random order); 0 = contiguous cache")
@@ -115,6 +119,9 @@ def recorded_traffic(workload):
 
 
 class ClockSampler:
+    """nvidia-smi sampling of SM clocks, power and throttle reasons (every
+    20 ms) for the whole run; summary(window) reports the samples that fall in
+    a host wall-clock window."""
     FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
@@ -136,33 +143,35 @@ class ClockSampler:
         except Exception:
             self.proc = None
 
-    def stop(self, window=None):
-        """Summarise the samples whose timestamps fall inside `window`
-        (host wall-clock seconds); all samples if none do."""
+    def _rows(self):
+        import datetime
+        rows = []
+        try:
+            with open(self.path) as fh:
+                for line in fh:
+                    parts = [p.strip() for p in line.split(",")]
+                    if len(parts) >= 10:
+                        try:
+                            ts = datetime.datetime.strptime(parts[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+                        except ValueError:
+                            ts = None
+                        rows.append((ts, parts[1:]))
+        except OSError:
+            pass
+        return rows
+
+    def summary(self, window=None):
+        """Samples whose timestamps fall inside `window` (host wall-clock
+        seconds), widened by one sampling period on each side; all samples so
+        far if none do."""
         if self.proc is None:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
-        self.proc.terminate()
-        try:
-            self.proc.wait(timeout=5)
-        except Exception:
-            self.proc.kill()
-        import datetime
-        rows, inside = [], []
-        with open(self.path) as fh:
-            for line in fh:
-                parts = [p.strip() for p in line.split(",")]
-                if len(parts) >= 10:
-                    try:
-                        ts = datetime.datetime.strptime(parts[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
-                    except ValueError:
-                        ts = None
-                    rows.append(parts[1:])
-                    if window and ts is not None and window[0] <= ts <= window[1]:
-                        inside.append(parts[1:])
-        os.unlink(self.path)
+        time.sleep(0.05)          # let the sample after the window be written
+        all_rows = self._rows()
+        inside = [r for ts, r in all_rows
+                  if window and ts is not None and window[0] - 0.02 <= ts <= window[1] + 0.02]
         in_window = bool(inside)
-        if inside:
-            rows = inside
+        rows = inside if inside else [r for _, r in all_rows]
         if not rows:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
 
@@ -180,6 +189,19 @@ class ClockSampler:
                 "sm_max_mhz": max(smax) if smax else None,
                 "reasons": reasons, "samples": len(rows), "in_timed_window": in_window,
                 "power_w_max": max((num(r[3]) or 0.0) for r in rows)}
+
+    def stop(self):
+        if self.proc is None:
+            return
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        try:
+            os.unlink(self.path)
+        except OSError:
+            pass
 
 
 def physical_gpu_index(local_rank):
@@ -285,79 +307,218 @@ def config_of(name, case, extra=None):
     return c
 
 
+class Runner:
+    """One workload's inputs on the device and its verify call through the C ABI.
+
+    The cache is rotated over enough copies that the working set exceeds
+    twice the L2, so every call reads its cache from HBM."""
+
+    def __init__(self, mva, name, dev, page_size=0):
+        import torch
+        self.mva, self.name, self.dev, self.page_size = mva, name, dev, page_size
+        self.case = case = I.make_case(I.WORKLOADS[name], pad="normal")
+
+        def t(a, dt):
+            return torch.from_numpy(np.ascontiguousarray(a)).view(dt).to(dev)
+
+        self.t = t
+        self.q_nope = t(case.q_nope.view(np.int16), torch.bfloat16)
+        self.q_rope = t(case.q_rope.view(np.int16), torch.bfloat16)
+        self.seq = t(case.seq_lens, torch.int32)
+        self.mask = t(case.mask.view(np.int32), torch.int32)
+        self.paged = page_size > 0
+        if self.paged:
+            self.pool, self.table = I.to_paged(case, page_size, seed=case_seed_for_pages(case),
+                                               extra_pages=0)
+            kv0 = t(self.pool.view(np.int16), torch.bfloat16)
+            self.table_d = t(self.table, torch.int32)
+        else:
+            kv0 = t(case.kv.view(np.int16), torch.bfloat16)
+        self.kv0 = kv0
+        self.l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+        self.kv_bytes = kv0.numel() * 2
+        self.copies = max(2, math.ceil(2.0 * self.l2 / self.kv_bytes) + 1)
+        self.kvs = [kv0] + [kv0.clone() for _ in range(self.copies - 1)]
+        B, q, H, Smax = case.B, case.q, case.H, case.Smax
+        if self.paged:
+            Smax = self.table.shape[1] * page_size      # the paged call's key bound
+        self.B, self.q, self.H, self.Smax = B, q, H, Smax
+        self.out = torch.empty((B, q, H, 512), dtype=torch.float32, device=dev)
+        self.lse = torch.empty((B, q, H), dtype=torch.float32, device=dev)
+        if self.paged:
+            self.need = mva.paged_workspace_size(B, q, H, self.table.shape[1], page_size)
+        else:
+            self.need = mva.workspace_size(B, q, H, Smax)
+        self.ws = torch.empty(max(self.need, 1), dtype=torch.uint8, device=dev)
+        self.n_rt, self.nsplit, self.chunk = mva.plan(B, q, H, Smax)
+        # split kernel; the slice merge when the keys are split; for pages that
+        # are not whole 64-key tiles the copy into a contiguous cache; the
+        # library's planner kernel for split calls with 2..32 streams (the
+        # bench never forces the slice count)
+        copied = self.paged and page_size % 64 != 0
+        planned = 2 <= B <= 32 and self.nsplit > 1
+        self.launches_per_call = (1 + (1 if self.nsplit > 1 else 0) + (1 if copied else 0)
+                                  + (1 if planned else 0))
+        self.stream = torch.cuda.current_stream(dev)
+        self.sh = int(self.stream.cuda_stream)
+        self.flops, self.cache_bytes = work_of(case)
+
+    def call(self, i, stream_handle=None):
+        mva, c = self.mva, self.case
+        sh = self.sh if stream_handle is None else stream_handle
+        if self.paged:
+            st = mva.load_library().mla_verify_attn_paged(
+                self.q_nope.data_ptr(), self.q_rope.data_ptr(), self.kvs[i % self.copies].data_ptr(),
+                self.kv0.shape[0], self.table_d.data_ptr(), self.table_d.shape[1], self.page_size,
+                self.seq.data_ptr(), self.mask.data_ptr(), self.B, self.q, self.H, float(c.scale),
+                self.out.data_ptr(), self.lse.data_ptr(), self.ws.data_ptr(), self.ws.numel(), sh)
+        else:
+            st = mva.verify_attn_raw(self.q_nope.data_ptr(), self.q_rope.data_ptr(),
+                                     self.kvs[i % self.copies].data_ptr(), self.seq.data_ptr(),
+                                     self.mask.data_ptr(), self.B, self.q, self.H, self.Smax,
+                                     float(c.scale), self.out.data_ptr(), self.lse.data_ptr(),
+                                     self.ws.data_ptr(), self.ws.numel(), sh)
+        if st != 0:
+            raise mva.MLAError(st)
+
+    def check_status(self, what):
+        st = self.mva.last_device_error()
+        if st != 0:
+            raise self.mva.MLAError(st, what)
+
+    def time_calls(self, n, first=0):
+        """us per call of n back-to-back calls (CUDA events on the call stream)."""
+        import torch
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(self.stream)
+        for i in range(n):
+            self.call(first + i)
+        e1.record(self.stream)
+        torch.cuda.synchronize(self.dev)
+        return e0.elapsed_time(e1) * 1e3 / n
+
+    def split_kernel_us(self, n):
+        """The split kernel's own duration: the library records a pair of events
+        around each of its launches (the merge then starts after it ends)."""
+        import torch
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(n)]
+        for a, b in evs:
+            a.record(self.stream)
+            b.record(self.stream)
+        torch.cuda.synchronize(self.dev)
+        try:
+            for i in range(n):
+                self.mva.set_timing_events(*evs[i])
+                self.call(i)
+        finally:
+            self.mva.set_timing_events()
+        torch.cuda.synchronize(self.dev)
+        return statistics.median(a.elapsed_time(b) * 1e3 for a, b in evs)
+
+    def roofline(self, split_us, call_us):
+        hbm_gbs, bf16_tf, peak_src = measured_peaks()
+        t_tensor = self.flops / (bf16_tf * 1e12)
+        t_hbm = self.cache_bytes / (hbm_gbs * 1e9)
+        tensor = t_tensor >= t_hbm
+        tflops = self.flops / (split_us * 1e-6) / 1e12
+        gbs = self.cache_bytes / (split_us * 1e-6) / 1e9
+        r = {"bound": "tensor" if tensor else "hbm",
+             "achieved": tflops if tensor else gbs,
+             "peak": bf16_tf if tensor else hbm_gbs,
+             "unit": "TFLOP/s" if tensor else "GB/s"}
+        r["frac"] = r["achieved"] / r["peak"]
+        r["effective_tflops"] = tflops
+        r["effective_gbs"] = gbs
+        r["roofline_us"] = max(t_tensor, t_hbm) * 1e6
+        r["peak_source"] = ("%s (MEASURED_PEAKS.json burst)" % peak_src if peak_src == "measured"
+                            else "fallback")
+        r["kernel_us"] = split_us
+        r["call_us"] = call_us
+        r["call_frac"] = (self.flops / (call_us * 1e-6) / 1e12 / bf16_tf if tensor else
+                          self.cache_bytes / (call_us * 1e-6) / 1e9 / hbm_gbs)
+        r["call_tflops"] = self.flops / (call_us * 1e-6) / 1e12
+        r["call_gbs"] = self.cache_bytes / (call_us * 1e-6) / 1e9
+        return r
+
+    def release(self):
+        self.kvs = None
+        self.kv0 = None
+
+
+def config_report(mva, dev, name, args, sampler):
+    """One entry of the per-workload table: median us/call over several windows
+    of back-to-back calls (each window >= 50 ms, so that clock samples fall
+    inside), the split kernel's own median duration, the roofline, and the
+    oracle timed on the host cores."""
+    import torch
+    r = Runner(mva, name, dev)
+    for i in range(max(3, args.warmup)):
+        r.call(i)
+    torch.cuda.synchronize(dev)
+    r.check_status("warm-up " + name)
+    probe = r.time_calls(max(3, min(50, args.steps)))
+    per_window = max(args.steps, int(math.ceil(50e3 / max(probe, 1.0))))
+    windows = []
+    t0 = time.time()
+    for w in range(args.config_windows):
+        windows.append(r.time_calls(per_window, first=w * per_window))
+    t1 = time.time()
+    r.check_status("timed windows " + name)
+    call_us = statistics.median(windows)
+    split_us = r.split_kernel_us(min(200, per_window))
+    r.check_status("split timing " + name)
+    entry = {
+        "B": r.B, "q_len": r.q, "H": r.H, "Smax": r.Smax,
+        "seq_lens": [int(x) for x in r.case.seq_lens],
+        "plan": {"row_tiles": r.n_rt, "nsplit": r.nsplit, "chunk_tiles": r.chunk},
+        "launches_per_call": r.launches_per_call,
+        "us_per_call": call_us, "us_per_call_windows": windows, "calls_per_window": per_window,
+        "split_kernel_us": split_us,
+        "flops_per_call": r.flops, "cache_bytes_per_call": r.cache_bytes,
+        "roofline": r.roofline(split_us, call_us),
+        "clocks": sampler.summary(window=(t0, t1)),
+    }
+    r.release()
+    if not args.no_cpu_baseline:
+        c_us, cores, what, _ = oracle_sample(r.case, args.cpu_budget_s)
+        s_us, s_rows = oracle_single_thread(r.case, min(5.0, args.cpu_budget_s / 4))
+        entry["oracle"] = {"all_cores_us_per_call": c_us, "cores": cores, "sample": what,
+                           "single_thread_us_per_call": s_us,
+                           "single_thread_sample": "%d query rows on one thread, scaled to the "
+                                                   "whole call" % s_rows}
+    torch.cuda.empty_cache()
+    return entry
+
+
 def run_ours(args, rank, world, local_rank):
     import torch
     import mla_verify_attention_gb300 as mva
     dev = torch.device("cuda", local_rank)
     torch.cuda.set_device(dev)
     mva.load_library()
-    case = I.make_case(I.WORKLOADS[args.workload], pad="normal")
+    sampler = ClockSampler(physical_gpu_index(local_rank))
+    sampler.start()
 
-    def t(a, dt):
-        return torch.from_numpy(np.ascontiguousarray(a)).view(dt).to(dev)
+    # ---- every workload (rank 0, one GPU): the per-config table.
+    configs = None
+    if rank == 0 and world == 1 and args.configs == "all":
+        configs = {}
+        for name in I.WORKLOADS:
+            configs[name] = config_report(mva, dev, name, args, sampler)
 
-    q_nope = t(case.q_nope.view(np.int16), torch.bfloat16)
-    q_rope = t(case.q_rope.view(np.int16), torch.bfloat16)
-    seq = t(case.seq_lens, torch.int32)
-    mask = t(case.mask.view(np.int32), torch.int32)
-    paged = args.page_size > 0
-    if paged:
-        pool, table = I.to_paged(case, args.page_size, seed=case_seed_for_pages(case), extra_pages=0)
-        kv0 = t(pool.view(np.int16), torch.bfloat16)
-        table_d = t(table, torch.int32)
-    else:
-        kv0 = t(case.kv.view(np.int16), torch.bfloat16)
-    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
-    kv_bytes = kv0.numel() * 2
-    copies = max(2, math.ceil(2.0 * l2 / kv_bytes) + 1)
-    kvs = [kv0] + [kv0.clone() for _ in range(copies - 1)]
-    B, q, H, Smax = case.B, case.q, case.H, case.Smax
-    if paged:
-        Smax = table.shape[1] * args.page_size      # the paged call's key bound
-    out = torch.empty((B, q, H, 512), dtype=torch.float32, device=dev)
-    lse = torch.empty((B, q, H), dtype=torch.float32, device=dev)
-    if paged:
-        need = mva.paged_workspace_size(B, q, H, table.shape[1], args.page_size)
-    else:
-        need = mva.workspace_size(B, q, H, Smax)
-    ws = torch.empty(max(need, 1), dtype=torch.uint8, device=dev)
-    n_rt, nsplit, chunk = mva.plan(B, q, H, Smax)
-    # split kernel, the slice merge when the keys are split, and for pages
-    # that are not whole 64-key tiles the copy into a contiguous cache
-    copied = paged and args.page_size % 64 != 0
-    # the library's planner kernel: split calls with 2..32 streams, slice count not forced
-    planned = 2 <= B <= 32 and 1 < nsplit <= 32 and int(os.environ.get("MLA_VERIFY_NSPLIT", "0") or 0) <= 0
-    launches_per_call = 1 + (1 if nsplit > 1 else 0) + (1 if copied else 0) + (1 if planned else 0)
-    stream = torch.cuda.current_stream(dev)
-    sh = int(stream.cuda_stream)
-    ptrs = [q_nope.data_ptr(), q_rope.data_ptr(), None, seq.data_ptr(), mask.data_ptr()]
-
-    def call(i, stream_handle=None):
-        sh_i = sh if stream_handle is None else stream_handle
-        if paged:
-            st = mva.load_library().mla_verify_attn_paged(
-                ptrs[0], ptrs[1], kvs[i % copies].data_ptr(), kv0.shape[0], table_d.data_ptr(),
-                table_d.shape[1], args.page_size, ptrs[3], ptrs[4], B, q, H, float(case.scale),
-                out.data_ptr(), lse.data_ptr(), ws.data_ptr(), ws.numel(), sh_i)
-        else:
-            st = mva.verify_attn_raw(ptrs[0], ptrs[1], kvs[i % copies].data_ptr(), ptrs[3], ptrs[4],
-                                     B, q, H, Smax, float(case.scale), out.data_ptr(),
-                                     lse.data_ptr(), ws.data_ptr(), ws.numel(), sh_i)
-        if st != 0:
-            raise mva.MLAError(st)
-
+    # ---- the headline workload: W warm-up calls, then exactly K timed calls.
+    r = Runner(mva, args.workload, dev, args.page_size)
+    case = r.case
     dist = world > 1
     if dist:
         import torch.distributed as tdist
     for i in range(max(3, args.warmup)):
-        call(i)
+        r.call(i)
     torch.cuda.synchronize(dev)
-    st = mva.last_device_error()
-    if st != 0:
-        raise mva.MLAError(st, "warm-up")
-
-    sampler = ClockSampler(physical_gpu_index(local_rank))
-    sampler.start()
+    r.check_status("warm-up")
+    stream = r.stream
     ev0 = torch.cuda.Event(enable_timing=True)
     ev1 = torch.cuda.Event(enable_timing=True)
     if dist:
@@ -366,37 +527,20 @@ def run_ours(args, rank, world, local_rank):
     t_wall0 = time.time()
     ev0.record(stream)
     for i in range(args.steps):
-        call(i)
+        r.call(i)
     ev1.record(stream)
     torch.cuda.synchronize(dev)
     t_wall1 = time.time()
     if dist:
         tdist.barrier()
-    clocks = sampler.stop(window=(t_wall0, t_wall1))
     ms = ev0.elapsed_time(ev1)
     us_call = max_over_ranks(ms * 1e3 / args.steps, world, dev)
-    st = mva.last_device_error()
-    if st != 0:
-        raise mva.MLAError(st, "timed region")
+    r.check_status("timed region")
+    clocks = sampler.summary(window=(t_wall0, t_wall1))
 
-    # ---- the dominant kernel's own duration: the library records a pair of
-    # events around each split-kernel launch (a second loop over the same
-    # rotating inputs; here the merge starts after the split kernel ends).
-    n_split = min(args.steps, 200)
-    split_evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-                 for _ in range(n_split)]
-    for a, b in split_evs:
-        a.record(stream)
-        b.record(stream)
-    torch.cuda.synchronize(dev)
-    try:
-        for i in range(n_split):
-            mva.set_timing_events(*split_evs[i])
-            call(i)
-    finally:
-        mva.set_timing_events()
-    torch.cuda.synchronize(dev)
-    split_us = sum(a.elapsed_time(b) for a, b in split_evs) * 1e3 / n_split
+    # ---- the dominant kernel's own duration (a second loop over the same
+    # rotating inputs; the merge then starts after the split kernel ends).
+    split_us = r.split_kernel_us(min(args.steps, 200))
 
     # ---- the same calls replayed from a CUDA graph (one call per cache copy
     # captured once): what a decode loop that captures its steps sees.  Context
@@ -404,12 +548,13 @@ def run_ours(args, rank, world, local_rank):
     graph = torch.cuda.CUDAGraph()
     gstream = torch.cuda.Stream(dev)
     gstream.wait_stream(stream)
+    ncap = min(r.copies, 64)
     with torch.cuda.stream(gstream):
         with torch.cuda.graph(graph, stream=gstream):
-            for i in range(copies):
-                call(i, int(gstream.cuda_stream))
+            for i in range(ncap):
+                r.call(i, int(gstream.cuda_stream))
     torch.cuda.synchronize(dev)
-    reps = max(1, min(args.steps, 500) // copies)
+    reps = max(1, min(args.steps, 500) // ncap)
     graph.replay()
     torch.cuda.synchronize(dev)
     g0 = torch.cuda.Event(enable_timing=True)
@@ -419,39 +564,38 @@ def run_ours(args, rank, world, local_rank):
         graph.replay()
     g1.record(stream)
     torch.cuda.synchronize(dev)
-    graph_us = g0.elapsed_time(g1) * 1e3 / (reps * copies)
-    st = mva.last_device_error()
-    if st != 0:
-        raise mva.MLAError(st, "graph replay")
+    graph_us = g0.elapsed_time(g1) * 1e3 / (reps * ncap)
+    r.check_status("graph replay")
     del graph
 
     # ---- the same call on one cache copy, which stays in L2 between calls
     # (context: `value` rotates copies so that every call reads HBM).
     n_hot = max(1, min(args.steps, 500))
     for _ in range(3):
-        call(0)
+        r.call(0)
     h0 = torch.cuda.Event(enable_timing=True)
     h1 = torch.cuda.Event(enable_timing=True)
     h0.record(stream)
     for _ in range(n_hot):
-        call(0)
+        r.call(0)
     h1.record(stream)
     torch.cuda.synchronize(dev)
     hot_us = h0.elapsed_time(h1) * 1e3 / n_hot
-    st = mva.last_device_error()
-    if st != 0:
-        raise mva.MLAError(st, "hot-L2 calls")
+    r.check_status("hot-L2 calls")
 
     # ---- end to end through the public API, from pinned host buffers
+    paged = r.paged
     host_in = [torch.from_numpy(np.ascontiguousarray(a)).pin_memory() for a in
                (case.q_nope.view(np.int16), case.q_rope.view(np.int16),
-                (pool if paged else case.kv).view(np.int16), case.seq_lens, case.mask.view(np.int32))
-               + ((table,) if paged else ())]
+                (r.pool if paged else case.kv).view(np.int16), case.seq_lens, case.mask.view(np.int32))
+               + ((r.table,) if paged else ())]
+    B, q, H = r.B, r.q, r.H
     h_out = torch.empty((B, q, H, 512), dtype=torch.float32).pin_memory()
     h_lse = torch.empty((B, q, H), dtype=torch.float32).pin_memory()
     d_in = [torch.empty(h.shape, dtype=h.dtype, device=dev) for h in host_in]
     h2d = sum(h.numel() * h.element_size() for h in host_in)
     d2h = h_out.numel() * 4 + h_lse.numel() * 4
+    ws = r.ws if r.need > 0 else None
 
     def e2e_step():
         for d, h in zip(d_in, host_in):
@@ -459,12 +603,12 @@ def run_ours(args, rank, world, local_rank):
         if paged:
             o, l = mva.verify_attn_paged(d_in[0].view(torch.bfloat16), d_in[1].view(torch.bfloat16),
                                          d_in[2].view(torch.bfloat16), d_in[5], args.page_size,
-                                         d_in[3], d_in[4], float(case.scale), out=out, lse=lse,
-                                         workspace=ws if need > 0 else None)
+                                         d_in[3], d_in[4], float(case.scale), out=r.out, lse=r.lse,
+                                         workspace=ws)
         else:
             o, l = mva.verify_attn(d_in[0].view(torch.bfloat16), d_in[1].view(torch.bfloat16),
                                    d_in[2].view(torch.bfloat16), d_in[3], d_in[4], float(case.scale),
-                                   out=out, lse=lse, workspace=ws if need > 0 else None)
+                                   out=r.out, lse=r.lse, workspace=ws)
         h_out.copy_(o, non_blocking=True)
         h_lse.copy_(l, non_blocking=True)
 
@@ -480,37 +624,26 @@ def run_ours(args, rank, world, local_rank):
     e1.record(stream)
     torch.cuda.synchronize(dev)
     e2e_us = e0.elapsed_time(e1) * 1e3 / n_e2e
+    sampler.stop()
 
-    flops, cache_bytes = work_of(case)
-    hbm_gbs, bf16_tf, peak_src = measured_peaks()
-    t_tensor = flops / (bf16_tf * 1e12)
-    t_hbm = cache_bytes / (hbm_gbs * 1e9)
-    # Dominant kernel: the split kernel does every MMA of the call.
-    if t_tensor >= t_hbm:
-        achieved = flops / (split_us * 1e-6) / 1e12
-        roof = {"bound": "tensor", "achieved": achieved, "peak": bf16_tf, "unit": "TFLOP/s",
-                "frac": achieved / bf16_tf}
-    else:
-        achieved = cache_bytes / (split_us * 1e-6) / 1e9
-        roof = {"bound": "hbm", "achieved": achieved, "peak": hbm_gbs, "unit": "GB/s",
-                "frac": achieved / hbm_gbs}
+    roof = r.roofline(split_us, us_call)
     roof["traffic"] = recorded_traffic(args.workload)
-    roof["peak_source"] = "%s (MEASURED_PEAKS.json burst)" % peak_src if peak_src == "measured" \
-        else "fallback"
-    roof["kernel"] = "verify_split_kernel (1 of %d launches per call)" % launches_per_call
-    roof["kernel_us"] = split_us
-    roof["call_us"] = us_call
-    roof["call_frac"] = (flops / (us_call * 1e-6) / 1e12) / bf16_tf if t_tensor >= t_hbm else \
-        (cache_bytes / (us_call * 1e-6) / 1e9) / hbm_gbs
-    roof["algorithmic"] = {"flops_per_launch": flops, "cache_bytes_per_launch": cache_bytes}
+    roof["kernel"] = "verify_split_kernel (1 of %d launches per call)" % r.launches_per_call
+    roof["algorithmic"] = {"flops_per_launch": r.flops, "cache_bytes_per_launch": r.cache_bytes}
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        c_us, cores, what, _ = oracle_sample(case, args.cpu_budget_s)
-        s_us, s_rows = oracle_single_thread(case, min(5.0, args.cpu_budget_s / 4))
+        if configs and args.workload in configs and "oracle" in configs[args.workload]:
+            o = configs[args.workload]["oracle"]
+            c_us, cores, what, s_us = (o["all_cores_us_per_call"], o["cores"], o["sample"],
+                                       o["single_thread_us_per_call"])
+            s_what = o["single_thread_sample"]
+        else:
+            c_us, cores, what, _ = oracle_sample(case, args.cpu_budget_s)
+            s_us, s_rows = oracle_single_thread(case, min(5.0, args.cpu_budget_s / 4))
+            s_what = "%d query rows on one thread, scaled to the whole call" % s_rows
         cpu = {"value": c_us, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": what,
-               "single_thread": {"value": s_us, "unit": UNIT,
-                                 "sample": "%d query rows on one thread, scaled to the whole call" % s_rows}}
+               "single_thread": {"value": s_us, "unit": UNIT, "sample": s_what}}
 
     if rank == 0:
         ref = PAGES_US.get(args.workload)
@@ -524,8 +657,8 @@ def run_ours(args, rank, world, local_rank):
             "dtype": "bf16", "data": "synthetic",
             "config": config_of(args.workload, case, {
                 "l2": "inputs larger than L2: %d rotating cache copies (%.0f MB > %.0f MB L2)" % (
-                    copies, copies * kv_bytes / 1e6, l2 / 1e6),
-                "plan": {"row_tiles": n_rt, "nsplit": nsplit, "chunk_tiles": chunk},
+                    r.copies, r.copies * r.kv_bytes / 1e6, r.l2 / 1e6),
+                "plan": {"row_tiles": r.n_rt, "nsplit": r.nsplit, "chunk_tiles": r.chunk},
                 "cache": ("paged: %d-key pages in seeded random order" % args.page_size) if paged
                 else "contiguous [B, Smax, 576]",
                 "parallelism": "replicas" if world > 1 else "single GPU",
@@ -533,13 +666,14 @@ def run_ours(args, rank, world, local_rank):
                                     "(RTX PRO 6000, fp32), context only" % ref) if ref else None}),
             "roofline": roof,
             "cpu_baseline": cpu,
-            "graph": {"us_per_call": graph_us, "calls": reps * copies,
+            "configs": configs,
+            "graph": {"us_per_call": graph_us, "calls": reps * ncap,
                       "what": "the same calls replayed from one captured CUDA graph (context)"},
             "hot_l2": {"us_per_call": hot_us, "calls": n_hot,
                        "what": "the same call on one cache copy, resident in L2 (context)"},
             "e2e": {"value": e2e_us, "unit": UNIT, "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h},
-            "gpu_launches": args.steps * launches_per_call,
+            "gpu_launches": args.steps * r.launches_per_call,
             "clocks": clocks,
         }
         print(json.dumps(line), flush=True)
