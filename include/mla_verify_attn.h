@@ -170,9 +170,8 @@ int mla_verify_attn_paged(const void* q_nope_abs, const void* q_rope, const void
  * by all calls on the device since it was last read.
  * Every internal pipeline wait gives up after 2 s; the call's kernels then
  * unwind (waiting, again bounded, for their own copies in flight) and leave
- * the context usable.  For testing that path, a non-empty environment
- * variable MLA_VERIFY_TEST_STALL other than "0" makes one work unit of each
- * later call withhold one of its cache loads.
+ * the context usable.  mla_verify_attn_set_test_controls can make one work
+ * unit withhold a cache load, to exercise that path.
  */
 int mla_verify_attn_last_device_error(cudaStream_t stream);
 
@@ -185,9 +184,8 @@ const char* mla_verify_attn_strerror(int status);
  *   nsplit       = number of key-range slices (1 = no split, no scratch),
  *   chunk_tiles  = 64-key tiles per slice.
  * `max_clusters` is the number of 2-CTA clusters that fit on the device at
- * once (pass <= 0 to query the current device).  Honours the environment
- * variable MLA_VERIFY_NSPLIT (a positive integer forces the slice count, for
- * testing the split path on small inputs).  For 2 to 32 streams (count not
+ * once (pass <= 0 to query the current device).  Honours a slice count forced
+ * with mla_verify_attn_set_test_controls.  For 2 to 32 streams (count not
  * forced) this is the largest plan: a one-block planning kernel of the call
  * may choose fewer slices from the device's seq_lens, and the slices then
  * start longest first.
@@ -195,6 +193,38 @@ const char* mla_verify_attn_strerror(int status);
  */
 int mla_verify_attn_plan(int B, int q_len, int H, int Smax, int max_clusters, int* n_row_tiles,
                          int* nsplit, int* chunk_tiles);
+
+/*
+ * Measurement aid; the pages have no counterpart.  While both events are
+ * non-NULL, every mla_verify_attn call records `before_split` on its stream
+ * just before the split kernel is launched and `after_split` just after it, so
+ * cudaEventElapsedTime(before_split, after_split) is the split kernel's own
+ * duration.  While they are set, the slice merge is launched without overlapping
+ * the split kernel's tail.  NULL, NULL switches recording off.  The events are
+ * the caller's (cudaEventCreate); the library only records them.  Set this only
+ * while no other thread is calling into the library.  Returns MLA_OK, or
+ * MLA_ERR_NULLPTR when exactly one event is NULL.
+ */
+int mla_verify_attn_set_timing_events(cudaEvent_t before_split, cudaEvent_t after_split);
+
+/*
+ * Test controls; the pages have no counterpart.  Process-wide settings that
+ * every later call reads (a relaxed atomic load per call, no environment
+ * lookup), meant for the library's own tests:
+ *   force_nsplit > 0  forces the number of key-range slices (at most one per
+ *                     64-key tile of Smax), so that small inputs exercise the
+ *                     split and merge path; it also changes what
+ *                     mla_verify_attn_plan and the workspace sizes report,
+ *                     and switches the device-side slice plan off.  0 restores
+ *                     the library's own plan.
+ *   stall != 0        makes work unit 0 of every later call withhold one of its
+ *                     cache loads: its bounded waits run out after 2 s, the
+ *                     call's kernels unwind and the device status reports
+ *                     MLA_ERR_DEVICE_TIMEOUT.  0 switches this off.
+ * Set these only while no call is being made from another thread.  Returns
+ * MLA_OK, or MLA_ERR_ARG for a negative force_nsplit (nothing changes then).
+ */
+int mla_verify_attn_set_test_controls(int force_nsplit, int stall);
 
 /*
  * mla_verify_attn without a caller-provided workspace.  This entry point has no
@@ -220,19 +250,6 @@ int mla_verify_attn_plan(int B, int q_len, int H, int Smax, int max_clusters, in
  * GPU (e.g. issued to two streams without ordering between them) race on the
  * array and may corrupt each other's results: order them, e.g. on one stream.
  */
-/*
- * Measurement aid; the pages have no counterpart.  While both events are
- * non-NULL, every mla_verify_attn call records `before_split` on its stream
- * just before the split kernel is launched and `after_split` just after it, so
- * cudaEventElapsedTime(before_split, after_split) is the split kernel's own
- * duration.  While they are set, the slice merge is launched without overlapping
- * the split kernel's tail.  NULL, NULL switches recording off.  The events are
- * the caller's (cudaEventCreate); the library only records them.  Set this only
- * while no other thread is calling into the library.  Returns MLA_OK, or
- * MLA_ERR_NULLPTR when exactly one event is NULL.
- */
-int mla_verify_attn_set_timing_events(cudaEvent_t before_split, cudaEvent_t after_split);
-
 #define MLA_VERIFY_NOALLOC_SCRATCH_BYTES ((size_t)32 << 20)
 int mla_verify_attn_noalloc(const void* q_nope_abs, const void* q_rope, const void* kv,
                             const int32_t* seq_lens, const uint32_t* tree_mask, int B, int q_len,

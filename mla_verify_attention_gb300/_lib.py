@@ -7,6 +7,7 @@ back to: if the library cannot be built or loaded, calls raise.
 """
 from __future__ import annotations
 
+import contextlib
 import ctypes
 import threading
 
@@ -21,7 +22,7 @@ STATUS_NAMES = {
 EXPORTED = ("mla_verify_attn", "mla_verify_attn_workspace_size", "mla_verify_attn_last_device_error",
             "mla_verify_attn_strerror", "mla_verify_attn_plan", "mla_verify_attn_paged",
             "mla_verify_attn_paged_workspace_size", "mla_verify_attn_set_timing_events",
-            "mla_verify_attn_noalloc")
+            "mla_verify_attn_set_test_controls", "mla_verify_attn_noalloc")
 
 _lock = threading.Lock()
 _lib = None
@@ -60,6 +61,10 @@ def load_library(build_if_missing: bool = True) -> ctypes.CDLL:
         lib.mla_verify_attn_paged_workspace_size.restype = Z
         lib.mla_verify_attn_set_timing_events.argtypes = [P, P]
         lib.mla_verify_attn_set_timing_events.restype = I
+        lib.mla_verify_attn_set_test_controls.argtypes = [I, I]
+        lib.mla_verify_attn_set_test_controls.restype = I
+        lib.mla_verify_attn_noalloc.argtypes = [P, P, P, P, P, I, I, I, I, F, P, P, P]
+        lib.mla_verify_attn_noalloc.restype = I
         _lib = lib
         return lib
 
@@ -197,6 +202,28 @@ def set_timing_events(before=None, after=None) -> None:
     st = int(load_library().mla_verify_attn_set_timing_events(b or None, a or None))
     if st != MLA_OK:
         raise MLAError(st, "mla_verify_attn_set_timing_events")
+
+
+_controls = [0, 0]   # the values last given to mla_verify_attn_set_test_controls
+
+
+@contextlib.contextmanager
+def forced(nsplit=None, stall=False):
+    """Within the block, calls use a forced slice count (``nsplit`` > 0) and/or
+    make one work unit withhold a cache load (``stall``); both are restored on
+    exit.  For tests of the split/merge and timeout paths."""
+    lib = load_library()
+    old = list(_controls)
+    new = [int(nsplit or 0), 1 if stall else 0]
+    st = int(lib.mla_verify_attn_set_test_controls(*new))
+    if st != MLA_OK:
+        raise MLAError(st, "mla_verify_attn_set_test_controls")
+    _controls[:] = new
+    try:
+        yield
+    finally:
+        lib.mla_verify_attn_set_test_controls(*old)
+        _controls[:] = old
 
 
 def last_device_error(stream=None) -> int:

@@ -5,9 +5,9 @@
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
 
+#include <atomic>
 #include <cmath>
 #include <cstdint>
-#include <cstdlib>
 #include <mutex>
 
 #include "mla_verify_attn.h"
@@ -29,15 +29,12 @@ constexpr int kMaxDevices = 64;
 // units fit one wave.
 constexpr int kMinTilesPerSlice = mla::kMinSliceTiles;
 // P precision.  Rounding P to one bf16 term (with the lazily kept row max)
-// put errors up to 4.8e-3 into outputs of streams of 4105..32760 keys, whose
-// few dominant keys carry much of each row's weight.  Caches of more than
-// kCorrectMaxKeys keys: streams up to kTwoTermMaxKeys send P as hi + lo.
-// Caches of up to kCorrectMaxKeys keys (the kCorrect kernel): streams up to
-// kTwoTermMaxKeysCorrected send hi + lo, longer ones one term plus the
-// correction of each row's dominant key.
-constexpr int kTwoTermMaxKeys = 32768;
-constexpr int kCorrectMaxKeys = 32768;
-constexpr int kTwoTermMaxKeysCorrected = 4096;
+// put errors up to 4.8e-3 into outputs of streams of 4105..32760 keys, and up
+// to ~3e-3 into longer streams where one key carries much of a row's weight.
+// Streams up to kTwoTermMaxKeys keys send P as hi + lo (their slices are short,
+// and the second PV product is cheap there); longer ones send one term plus
+// the correction of each row's dominant key (the kCorrect kernel).
+constexpr int kTwoTermMaxKeys = 4096;
 constexpr size_t kSmemBytes = sizeof(mla::Smem) + 1024;   // + manual 1 KB alignment
 
 struct DeviceInfo {
@@ -55,6 +52,11 @@ DeviceInfo g_devices[kMaxDevices];
 // Events recorded around the split kernel (mla_verify_attn_set_timing_events).
 cudaEvent_t g_timing_before = nullptr;
 cudaEvent_t g_timing_after = nullptr;
+
+// Test controls (mla_verify_attn_set_test_controls): a forced slice count
+// (0 = the plan's own) and the stall of one work unit; plain loads per call.
+std::atomic<int> g_force_nsplit{0};
+std::atomic<int> g_test_stall{0};
 
 int device_info(DeviceInfo** out) {
   int dev = -1;
@@ -130,8 +132,7 @@ int plan(int B, int q, int H, int Smax, int max_clusters, int* n_rt, int* nsplit
   const int tiles = (Smax + mla::kKeys - 1) / mla::kKeys;
   const long long base = static_cast<long long>(B > 0 ? B : 1) * nrt;
   long long ns;
-  const char* env = std::getenv("MLA_VERIFY_NSPLIT");
-  const long long forced = env ? std::atoll(env) : 0;
+  const long long forced = g_force_nsplit.load(std::memory_order_relaxed);
   int ct;
   if (forced > 0) {
     ns = forced < tiles ? forced : tiles;
@@ -168,10 +169,7 @@ size_t workspace_bytes_for(int B, int q, int H, int nsplit) {
   return plan_offset(B, q, H, nsplit) + 256;
 }
 
-bool nsplit_forced() {
-  const char* env = std::getenv("MLA_VERIFY_NSPLIT");
-  return env && std::atoll(env) > 0;
-}
+bool nsplit_forced() { return g_force_nsplit.load(std::memory_order_relaxed) > 0; }
 
 // Calls whose slice count plan_kernel chooses from the stream lengths: split
 // calls with 2 to 32 streams, unless the count is forced.
@@ -384,13 +382,12 @@ int run(const Call& c) {
                                                          plan_offset(B, q_len, H, ns))
                                 : nullptr;
   p.plan = plan_dev;
-  const bool corrected = Smax <= kCorrectMaxKeys;
-  const int two_term_max_keys = corrected ? kTwoTermMaxKeysCorrected : kTwoTermMaxKeys;
+  const bool corrected = true;
+  const int two_term_max_keys = kTwoTermMaxKeys;
   p.two_term_max_keys = two_term_max_keys;
   p.kv = static_cast<const uint8_t*>(kv);
   p.kv_rows = paged ? c.pool_rows : static_cast<long long>(Smax);
-  const char* stall = std::getenv("MLA_VERIFY_TEST_STALL");
-  p.test_stall = (stall && stall[0] && stall[0] != '0') ? 1 : 0;
+  p.test_stall = g_test_stall.load(std::memory_order_relaxed) != 0 ? 1 : 0;
   p.scale_log2 = scale * 1.4426950408889634f;
   p.block_table = paged ? c.block_table : nullptr;
   p.max_blocks = paged ? c.max_blocks : 0;
@@ -548,6 +545,31 @@ int mla_verify_attn_set_timing_events(cudaEvent_t before_split, cudaEvent_t afte
   if ((before_split == nullptr) != (after_split == nullptr)) return MLA_ERR_NULLPTR;
   g_timing_before = before_split;
   g_timing_after = after_split;
+  return MLA_OK;
+}
+
+#ifdef MLA_TRACE
+// Trace builds only (not part of the ABI): copies the split kernel's timeline
+// buffers of the current device to the host and clears them.
+int mla_verify_attn_trace_read(unsigned long long* tiles, unsigned long long* spans) {
+  if (cudaDeviceSynchronize() != cudaSuccess) return MLA_ERR_LAUNCH;
+  if (cudaMemcpyFromSymbol(tiles, mla::g_trace_tiles, sizeof(mla::g_trace_tiles)) != cudaSuccess ||
+      cudaMemcpyFromSymbol(spans, mla::g_trace_spans, sizeof(mla::g_trace_spans)) != cudaSuccess)
+    return MLA_ERR_LAUNCH;
+  void* p = nullptr;
+  if (cudaGetSymbolAddress(&p, mla::g_trace_tiles) != cudaSuccess ||
+      cudaMemset(p, 0, sizeof(mla::g_trace_tiles)) != cudaSuccess ||
+      cudaGetSymbolAddress(&p, mla::g_trace_spans) != cudaSuccess ||
+      cudaMemset(p, 0, sizeof(mla::g_trace_spans)) != cudaSuccess)
+    return MLA_ERR_LAUNCH;
+  return MLA_OK;
+}
+#endif
+
+int mla_verify_attn_set_test_controls(int force_nsplit, int stall) {
+  if (force_nsplit < 0) return MLA_ERR_ARG;
+  g_force_nsplit.store(force_nsplit, std::memory_order_relaxed);
+  g_test_stall.store(stall != 0 ? 1 : 0, std::memory_order_relaxed);
   return MLA_OK;
 }
 

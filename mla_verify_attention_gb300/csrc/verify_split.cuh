@@ -115,6 +115,56 @@ enum : uint32_t { kCmdDone = 0xFFFFFFFFu, kCmdZeroTail = 0x80000000u };
 // Device status bits (first error wins in the host's report).
 enum : uint32_t { kStatusSeqLen = 1u, kStatusTimeout = 2u, kStatusPage = 4u };
 
+// Optional timeline of the split kernel (a build with -DMLA_TRACE; the
+// library's normal build compiles every stamp away).  %globaltimer stamps, in
+// ns: per tile j of the first kTraceUnits work units, the moments each role
+// passed its pipeline waits (kTrace* below), and per CTA of every unit (up to
+// kTraceSpanUnits) the moments it passed the prologue, loop and epilogue.
+#ifdef MLA_TRACE
+constexpr int kTraceUnits = 8, kTraceEvents = 10, kTraceTiles = 128, kTraceSpanUnits = 1024;
+constexpr int kTraceSpans = 12;
+__device__ unsigned long long g_trace_tiles[kTraceUnits][2][kTraceEvents][kTraceTiles];
+__device__ unsigned long long g_trace_spans[kTraceSpanUnits][2][kTraceSpans];
+#define MLA_TRACE_TILE(ev, j)                                                           \
+  do {                                                                                  \
+    const int u_ = static_cast<int>(blockIdx.x >> 1);                                   \
+    if (u_ < kTraceUnits && (j) < kTraceTiles)                                          \
+      g_trace_tiles[u_][blockIdx.x & 1][ev][j] = globaltimer_ns();                      \
+  } while (0)
+#define MLA_TRACE_SPAN(ev)                                                              \
+  do {                                                                                  \
+    const int u_ = static_cast<int>(blockIdx.x >> 1);                                   \
+    if (u_ < kTraceSpanUnits) g_trace_spans[u_][blockIdx.x & 1][ev] = globaltimer_ns(); \
+  } while (0)
+#else
+#define MLA_TRACE_TILE(ev, j) do {} while (0)
+#define MLA_TRACE_SPAN(ev) do {} while (0)
+#endif
+// Tile events: S CTA (rank 0) / O CTA (rank 1).
+enum {
+  kTrQK0 = 0,      // S MMA warp: key tile part 0 landed, QK(j) starts
+  kTrQK1 = 1,      //   part 1 landed
+  kTrQKIssued = 2, //   QK(j) issued and committed
+  kTrSoftIn = 3,   // S softmax (warp 4, lane 0): scores of tile j in registers
+  kTrStaged = 4,   //   P(j) staged, before the per-tile barrier
+  kTrBarrier = 5,  //   past the per-tile barrier
+  kTrCopy = 6,     // S copy issuer: O's P buffer free, P(j) copy issued
+  kTrKLoad0 = 7,   // S producer: part 0 of key tile j issued (slot free)
+  kTrKLoad1 = 8,   //   part 1 issued
+  kTrPFull = 0,    // O MMA warp: P(j) landed
+  kTrVFull = 1,    //   value tile j landed
+  kTrPVIssued = 2, //   PV(j) issued and committed
+  kTrVLoad = 3,    // O producer: value slot free, tile j issued
+};
+// Spans (per CTA): entry, prologue done (after the cluster sync), Q landed (S)
+// / -, Q in tensor memory (S) / -, main loop done, results ready for the
+// epilogue (O), epilogue stores complete (O), exit; within the prologue: unit
+// decoded, barriers initialised and first loads issued, tensor memory
+// allocated, CTA barrier passed.
+enum { kSpEntry = 0, kSpSynced = 1, kSpQLanded = 2, kSpQReady = 3, kSpLoopDone = 4,
+       kSpEpiReady = 5, kSpEpiDone = 6, kSpExit = 7, kSpDecoded = 8, kSpIssued = 9,
+       kSpAlloc = 10, kSpCtaSync = 11 };
+
 struct SplitParams {
   const int32_t* seq_lens;
   const uint32_t* mask;
@@ -130,7 +180,7 @@ struct SplitParams {
   // the page pool, with page_size a multiple of 64 (no tile crosses a page).
   const int32_t* block_table;   // [B][max_blocks]
   int max_blocks, page_size, pool_pages;
-  // Test hook (MLA_VERIFY_TEST_STALL): unit 0 never loads the second part of
+  // Test control (mla_verify_attn_set_test_controls): unit 0 never loads the second part of
   // key tile 0, so its bounded waits run out and report MLA_ERR_DEVICE_TIMEOUT.
   int test_stall;
   // Calls with 2..kOrderedStreams streams: {chunk_tiles, nsplit} chosen by
@@ -394,6 +444,7 @@ __device__ __forceinline__ void s_producer(Smem& sm, const Unit& u, const SplitP
       if (!wait_or_abort(sm, smem_u32(&sm.kempty[part][slot]), ((j / kKSlots) & 1) ^ 1, p, 2))
         return;
       s_issue_part(sm, map_kv0, map_kv1, org, j, part, n_issued);
+      MLA_TRACE_TILE(kTrKLoad0 + part, j);
     }
   }
 }
@@ -414,6 +465,7 @@ __device__ __forceinline__ void s_mma(Smem& sm, const Unit& u, const SplitParams
     // Descriptor of chunk c = descriptor of chunk 0 + c * 8 KB (in 16-byte units).
     const uint64_t bdesc0 = sdesc_sw128(ring + slot * kKTile, 16, 1024);
     if (!warp_wait(sm, smem_u32(&sm.kfull[0][slot]), (j / kKSlots) & 1, p, 5)) return;
+    if ((threadIdx.x & 31) == 0) MLA_TRACE_TILE(kTrQK0, j);
     tc_fence_after();
 #pragma unroll
     for (int c = 0; c < kKSplit; ++c)
@@ -421,6 +473,7 @@ __device__ __forceinline__ void s_mma(Smem& sm, const Unit& u, const SplitParams
                          kIdescQK, c != 0);
     mma_commit_elect(smem_u32(&sm.kempty[0][slot]));
     if (!warp_wait(sm, smem_u32(&sm.kfull[1][slot]), (j / kKSlots) & 1, p, 5)) return;
+    if ((threadIdx.x & 31) == 0) MLA_TRACE_TILE(kTrQK1, j);
     tc_fence_after();
 #pragma unroll
     for (int c = kKSplit; c < kKChunks; ++c)
@@ -428,6 +481,7 @@ __device__ __forceinline__ void s_mma(Smem& sm, const Unit& u, const SplitParams
                          kIdescQK, 1u);
     mma_commit_elect(smem_u32(&sm.kempty[1][slot]));
     mma_commit_elect(smem_u32(&sm.sfull[buf]));
+    if ((threadIdx.x & 31) == 0) MLA_TRACE_TILE(kTrQKIssued, j);
   }
 }
 
@@ -458,6 +512,7 @@ __device__ __forceinline__ void s_softmax(Smem& sm, const Unit& u, const SplitPa
   // moves four or five of the nine 64-dim chunks of its row).  All exits of
   // the softmax warps are taken together (they share named barriers).
   const bool qok = warp_wait(sm, smem_u32(&sm.qfull), 0, p, 6);
+  if (wq == 0 && half == 0 && lane == 0) MLA_TRACE_SPAN(kSpQLanded);
   if (named_bar_red_or(kSoftmaxBar, kRowThreads, !qok)) return;
   for (int c = half; c < kKChunks; c += 2) {
     const uint8_t* src = sm.ring + kQStage + c * kQChunk + r * 128;
@@ -476,6 +531,7 @@ __device__ __forceinline__ void s_softmax(Smem& sm, const Unit& u, const SplitPa
   tc_fence_before();
   __syncwarp();
   if (lane == 0) mbar_arrive(smem_u32(&sm.qready));
+  if (wq == 0 && half == 0 && lane == 0) MLA_TRACE_SPAN(kSpQReady);
 
   // ---- peer (O CTA) addresses: the exchange buffers sit at the same offsets
   const uint32_t peer = 1;
@@ -539,6 +595,7 @@ __device__ __forceinline__ void s_softmax(Smem& sm, const Unit& u, const SplitPa
   for (int j = 0; j < u.ntiles; ++j) {
     const int buf = j & 1;
     const bool got = warp_wait(sm, smem_u32(&sm.sfull[buf]), (j >> 1) & 1, p, 7);
+    if (wq == 0 && half == 0 && lane == 0) MLA_TRACE_TILE(kTrSoftIn, j);
     uint32_t sr[32];
     float mh = -CUDART_INF_F;   // this half's tile max (log2-scaled)
     float mraw = -CUDART_INF_F; // the same before the scale (kCorrect)
@@ -553,6 +610,7 @@ __device__ __forceinline__ void s_softmax(Smem& sm, const Unit& u, const SplitPa
 #pragma unroll
         for (int c = 0; c < 32; ++c) sr[c] = __float_as_uint(__uint_as_float(sr[c]) * a);
       }
+
       // Keys wholly inside the prefix are visible; otherwise bit c of `vis`
       // says whether key key0+c is visible to this row.
       const int key0 = u.k0 + j * kKeys + 32 * half;
@@ -595,7 +653,10 @@ __device__ __forceinline__ void s_softmax(Smem& sm, const Unit& u, const SplitPa
     fence_proxy_async_smem();
     // One barrier per tile: any overflowing row, or any failed wait.  Only
     // then (rarely) a second one tells the two apart.
-    if (named_bar_red_or(kSoftmaxBar, kRowThreads, ovf || !got || copy_failed)) {
+    if (wq == 0 && half == 0 && lane == 0) MLA_TRACE_TILE(kTrStaged, j);
+    const bool any_ovf = named_bar_red_or(kSoftmaxBar, kRowThreads, ovf || !got || copy_failed);
+    if (wq == 0 && half == 0 && lane == 0) MLA_TRACE_TILE(kTrBarrier, j);
+    if (any_ovf) {
       if (named_bar_red_or(kSoftmaxBar, kRowThreads, !got || copy_failed)) {
         finished = false;
         break;
@@ -627,6 +688,7 @@ __device__ __forceinline__ void s_softmax(Smem& sm, const Unit& u, const SplitPa
     if (half == 0 && r == 0) {
       // The O CTA's buffer `buf` is free once its PV product of tile j-2 is done.
       if (wait_or_abort<true>(sm, smem_u32(&sm.pempty[buf]), ((j >> 1) & 1) ^ 1, p, 8)) {
+        MLA_TRACE_TILE(kTrCopy, j);
         bulk_copy_to_peer(xbuf0_remote + buf * kPBuf, xbuf0 + buf * kPBuf, xbytes,
                           buf ? pfull_remote1 : pfull_remote0);
         bulk_commit_group();
@@ -655,6 +717,7 @@ __device__ __forceinline__ void s_softmax(Smem& sm, const Unit& u, const SplitPa
     }
   }
   if (half == 0 && r == 0) bulk_wait_read<0>();
+  if (wq == 0 && half == 0 && lane == 0) MLA_TRACE_SPAN(kSpLoopDone);
   if (!finished) return;
   if (half == 1) {
     sm.xl[r] = l;
@@ -719,6 +782,7 @@ __device__ __forceinline__ void o_producer(Smem& sm, const Unit& u, const SplitP
     const int slot = j & 1;
     if (!wait_or_abort(sm, smem_u32(&sm.vempty[slot]), ((j >> 1) & 1) ^ 1, p, 9)) return;
     o_issue(sm, map_kv, org, j, n_issued);
+    MLA_TRACE_TILE(kTrVLoad, j);
   }
 }
 
@@ -749,9 +813,11 @@ __device__ __forceinline__ void o_mma(Smem& sm, const Unit& u, const SplitParams
     const int buf = j & 1;
     const int slot = j & 1;
     if (!warp_wait<true>(sm, smem_u32(&sm.pfull[buf]), (j >> 1) & 1, p, 11)) break;
+    if (lane == 0) MLA_TRACE_TILE(kTrPFull, j);
     if (lane == 0 && j + 2 < u.ntiles) mbar_arrive_expect_tx(smem_u32(&sm.pfull[buf]), pbytes);
     fence_proxy_async_smem();
     if (!warp_wait(sm, smem_u32(&sm.vfull[slot]), (j >> 1) & 1, p, 12)) break;
+    if (lane == 0) MLA_TRACE_TILE(kTrVFull, j);
     if (j == u.ntiles - 1 && u.zero_tail) {
       if (!o_command(sm, kCmdZeroTail | static_cast<uint32_t>(j), ncmd, p, lane)) break;
     }
@@ -782,8 +848,10 @@ __device__ __forceinline__ void o_mma(Smem& sm, const Unit& u, const SplitParams
     }
     mma_commit_elect(smem_u32(&sm.vempty[slot]));
     mma_commit_mc_elect(smem_u32(&sm.pempty[buf]), static_cast<uint16_t>(1u));  // rank 0 = S CTA
+    if (lane == 0) MLA_TRACE_TILE(kTrPVIssued, j);
   }
   mma_commit_elect(smem_u32(&sm.odone));
+  if (lane == 0) MLA_TRACE_SPAN(kSpLoopDone);
   if (lane == 0) {
     *reinterpret_cast<volatile uint32_t*>(&sm.cmd) = kCmdDone;
     mbar_arrive(smem_u32(&sm.corrgo));
@@ -913,6 +981,7 @@ __device__ __forceinline__ void o_helpers(Smem& sm, const Unit& u, const SplitPa
             warp_wait<true>(sm, smem_u32(&sm.mlfull), 0, p, 16);
   }
   if (named_bar_red_or(bar, kRows, !ready)) return;
+  if (tid == 0) MLA_TRACE_SPAN(kSpEpiReady);
   tc_fence_after();
   const float2 ml = sm.ml[r];
   const bool valid = r < u.valid_rows;
@@ -987,6 +1056,7 @@ __device__ __forceinline__ void o_helpers(Smem& sm, const Unit& u, const SplitPa
     if (cc + 1 < 8) tmem_ld_wait();
   }
   if (issuer) bulk_wait_all();
+  if (issuer && half == 0) MLA_TRACE_SPAN(kSpEpiDone);
   tc_fence_before();
 }
 
@@ -1019,7 +1089,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   const int warp = tid >> 5;
   const int lane = tid & 31;
   const uint32_t role = cluster_ctarank();   // 0: scores + softmax, 1: PV accumulator
+  if (tid == 0) MLA_TRACE_SPAN(kSpEntry);
   const Unit u = decode_unit(p);
+  if (tid == 0) MLA_TRACE_SPAN(kSpDecoded);
   const bool corr = kCorrect && !u.two_term;   // one-term P plus the dominant-key correction
   // The slice merge is launched as a programmatic dependent of this grid; it
   // may be scheduled now and waits for this grid's completion itself.
@@ -1069,6 +1141,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     }
     fence_mbarrier_init_cluster();
     fence_proxy_async_smem();   // the initialised barriers, before TMA completes on them
+  }
+  // Arrive on the cluster barrier as soon as the barriers are initialised; the
+  // wait below (before any access to the peer CTA) overlaps the first loads
+  // and the tensor-memory allocation.
+  cluster_arrive_relaxed();
+  if (tid == 0) {
     if (!u.empty) {
       if (role == 0) {
         if (p.block_table != nullptr)
@@ -1083,15 +1161,19 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           o_producer_start<false, kAfterCopy>(sm, u, p, &map_kvo, n_issued[0]);
       }
     }
+    MLA_TRACE_SPAN(kSpIssued);
   }
   if (!u.empty && warp == 2) {
     tmem_alloc(smem_u32(&sm.tmem_base), 512);
     tmem_relinquish();
+    if (lane == 0) MLA_TRACE_SPAN(kSpAlloc);
   }
   tc_fence_before();
   __syncthreads();
-  cluster_sync_all();
+  if (tid == 0) MLA_TRACE_SPAN(kSpCtaSync);
+  cluster_wait();
   tc_fence_after();
+  if (tid == 0) MLA_TRACE_SPAN(kSpSynced);
   const uint32_t tmem = sm.tmem_base;
 
   if (!u.empty) {
@@ -1139,6 +1221,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     tc_fence_after();
     tmem_dealloc(tmem, 512);
   }
+  if (tid == 0) MLA_TRACE_SPAN(kSpExit);
   cluster_sync_all();
 }
 

@@ -89,11 +89,17 @@ def test_plan_arithmetic(lib):
     assert mva.plan(2, 3, 16, 1000, 76)[0] == 1
 
 
-def test_plan_env_override(lib, monkeypatch):
-    monkeypatch.setenv("MLA_VERIFY_NSPLIT", "3")
-    assert mva.plan(1, 9, 64, 320, 76) == (5, 3, 2)
+def test_forced_slice_count(lib, monkeypatch):
+    with mva.forced(nsplit=3):
+        assert mva.plan(1, 9, 64, 320, 76) == (5, 3, 2)
+    with mva.forced(nsplit=100):
+        assert mva.plan(1, 9, 64, 320, 76) == (5, 5, 1)
+    assert mva.plan(1, 9, 64, 320, 76) == (5, 3, 2)          # own plan again
+    # the environment is never consulted
     monkeypatch.setenv("MLA_VERIFY_NSPLIT", "100")
-    assert mva.plan(1, 9, 64, 320, 76) == (5, 5, 1)
+    assert mva.plan(1, 9, 64, 4160, 76) == (5, 13, 5)
+    assert lib.mla_verify_attn_set_test_controls(-1, 0) == -9   # MLA_ERR_ARG
+    assert mva.plan(1, 9, 64, 4160, 76) == (5, 13, 5)
 
 
 def paged(lib, **kw):

@@ -1,7 +1,7 @@
 """Failure detection and memory discipline on the GPU, without faulting it.
 
-- A stalled pipeline: the test hook MLA_VERIFY_TEST_STALL makes one work unit
-  withhold a cache load; its bounded waits run out (2 s), the kernels unwind,
+- A stalled pipeline: the library's test control (mla_verify_attn_set_test_controls)
+  makes one work unit withhold a cache load; its bounded waits run out (2 s), the kernels unwind,
   the device status reports MLA_ERR_DEVICE_TIMEOUT, and the next call on the
   same context is correct.
 - Guard bands: out, lse and the workspace are surrounded by sentinel bytes
@@ -39,17 +39,16 @@ def _check(case, out, lse):
     assert np.abs(l - ref_lse).max() <= TOL_LSE
 
 
-def test_stalled_pipeline_reports_timeout_and_recovers(monkeypatch):
+def test_stalled_pipeline_reports_timeout_and_recovers():
     import torch
     import mla_verify_attention_gb300 as mva
     case = I.make_case(I.WORKLOADS["chain9_p256"])
     inputs = _dev(case)
     assert mva.last_device_error() == 0
-    monkeypatch.setenv("MLA_VERIFY_TEST_STALL", "1")
-    mva.verify_attn(*inputs, float(case.scale))        # enqueued: the stall is device-side
-    torch.cuda.synchronize()
+    with mva.forced(stall=True):
+        mva.verify_attn(*inputs, float(case.scale))    # enqueued: the stall is device-side
+        torch.cuda.synchronize()
     assert mva.last_device_error() == -7               # MLA_ERR_DEVICE_TIMEOUT, then cleared
-    monkeypatch.delenv("MLA_VERIFY_TEST_STALL")
     out, lse = mva.verify_attn(*inputs, float(case.scale))
     torch.cuda.synchronize()
     assert mva.last_device_error() == 0
@@ -61,11 +60,15 @@ GUARD = 4096      # bytes on each side (keeps the 256-byte workspace alignment)
 
 @pytest.mark.parametrize("name,nsplit", [("tree9_p4096", None), ("chain9_p256", 1),
                                          ("ragged8_tree9", None)])
-def test_guard_bands_untouched(name, nsplit, monkeypatch):
+def test_guard_bands_untouched(name, nsplit):
+    import mla_verify_attention_gb300 as mva
+    with mva.forced(nsplit=nsplit):
+        _guard_bands(name, nsplit)
+
+
+def _guard_bands(name, nsplit):
     import torch
     import mla_verify_attention_gb300 as mva
-    if nsplit is not None:
-        monkeypatch.setenv("MLA_VERIFY_NSPLIT", str(nsplit))
     case = I.make_case(I.WORKLOADS[name])
     B, q, H, Smax = case.B, case.q, case.H, case.Smax
     n_out, n_lse = B * q * H * 512 * 4, B * q * H * 4

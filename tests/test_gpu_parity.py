@@ -4,8 +4,6 @@ Tolerances (fixed for this path): max |out - oracle| <= 2e-3 and
 max |lse - oracle| <= 1e-3.  Cache rows past each stream's length are NaN in
 every case here and must have no influence.
 """
-import os
-
 import numpy as np
 import pytest
 
@@ -33,19 +31,10 @@ def to_dev(case):
 def run_gpu(case, nsplit=None):
     import torch
     import mla_verify_attention_gb300 as mva
-    old = os.environ.get("MLA_VERIFY_NSPLIT")
-    if nsplit is not None:
-        os.environ["MLA_VERIFY_NSPLIT"] = str(nsplit)
-    try:
+    with mva.forced(nsplit=nsplit):
         out, lse = mva.verify_attn(*to_dev(case), float(case.scale))
         torch.cuda.synchronize()
         st = mva.last_device_error()
-    finally:
-        if nsplit is not None:
-            if old is None:
-                os.environ.pop("MLA_VERIFY_NSPLIT", None)
-            else:
-                os.environ["MLA_VERIFY_NSPLIT"] = old
     assert st == 0, mva.strerror(st)
     return out.cpu().numpy().astype(np.float64), lse.cpu().numpy().astype(np.float64)
 
@@ -255,18 +244,47 @@ def test_deterministic():
     np.testing.assert_array_equal(a[1], b[1])
 
 
+# ---------------------------------------------------------------- Smax not a multiple of 64
+
+@pytest.mark.parametrize("B,prefixes,nsplit", [
+    (1, [4096], None),              # seq_len = Smax = 4105: the last key box runs past the cache
+    (1, [4096], 1),                 # same, one slice: normalised output written directly
+    (3, [100, 991, 500], None),     # Smax = 1000, ragged, device plan over 2..32 streams
+    (3, [100, 991, 500], 4),        # same, forced slices
+    (3, [100, 991, 500], 1),        # same, unsplit
+    (2, [40000, 31], None),         # Smax = 40009 (> 32768 keys), stream strides of 40009 rows
+])
+def test_smax_not_multiple_of_tile(B, prefixes, nsplit):
+    case = custom_case(B, 9, 64, prefixes, seed=1234 + sum(prefixes) + (nsplit or 0), smax_align=1)
+    assert case.Smax % 64 != 0
+    check(case, *run_gpu(case, nsplit=nsplit))
+
+
+# ---------------------------------------------------------------- dominant keys in large caches
+
+# One planted key per listed stream (its rope part scaled, so that it carries a
+# large share of many rows' weight) in caches of more than 32768 keys: the
+# 64k-prefix shape, a 40000-key stream, and a ragged 8-stream batch with one
+# stream longer than 32768 keys.  Its weight's bf16 rounding must not show.
+@pytest.mark.parametrize("B,prefixes,planted,factor,seed", [
+    (1, [65536], [(0, 40000)], 8.0, 21),
+    (1, [65536], [(0, 61000)], 10.0, 22),
+    (1, [39991], [(0, 20000)], 8.0, 23),
+    (1, [39991], [(0, 39000)], 10.0, 24),
+    (8, [1500, 40000, 3000, 9000, 20000, 1100, 30000, 6000],
+     [(1, 35000), (3, 8000), (4, 100), (6, 29000)], 8.0, 25),
+])
+def test_dominant_key_in_large_cache(B, prefixes, planted, factor, seed):
+    case = custom_case(B, 9, 64, prefixes, seed)
+    assert case.Smax > 32768
+    for b, key in planted:
+        I.scale_key_rope(case, b, key, factor)
+    check(case, *run_gpu(case))
+
+
 # ---------------------------------------------------------------- full-size workloads
 
-def sampled_rows(case, n=3):
-    rows = case.B * case.q * case.H
-    starts = np.linspace(0, rows - 64, n).astype(int)
-    return [(int(s), 64) for s in starts]
-
-
 @pytest.mark.parametrize("name", ["tree33_p16384", "tree9_p65536", "ragged8_tree9"])
-def test_full_size_sampled(name):
+def test_full_size_every_row(name):
     case = I.make_case(I.WORKLOADS[name])
-    out, lse = run_gpu(case)
-    assert np.isfinite(out).all() and np.isfinite(lse).all()
-    for rows in sampled_rows(case):
-        check(case, out, lse, rows=rows)
+    check(case, *run_gpu(case))

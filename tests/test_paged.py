@@ -66,6 +66,22 @@ def test_paged_matches_oracle(B, q, H, prefixes, page_size):
     check(case, out, lse)
 
 
+@pytest.mark.parametrize("B,prefixes,page_size", [
+    (1, [991], 16),                 # Smax = 1000 keys: 63 pages of 16 = 1008 keys
+    (3, [100, 991, 500], 7),        # 143 pages of 7 = 1001 keys, ragged
+    (1, [4096], 48),                # 86 pages of 48 = 4128 keys, split path
+])
+def test_paged_smax_not_multiple_of_tile(B, prefixes, page_size):
+    # The copied cache then has a row count that is not a whole number of
+    # 64-key tiles: the last key box of a stream runs past it.
+    w = I.Workload("paged", B, 9, 0, "random", 5, None, H=64)
+    case = I.make_case(w, seed=77 + page_size, prefixes=prefixes, smax_align=1)
+    max_blocks = -(-case.Smax // page_size)
+    assert (max_blocks * page_size) % 64 != 0
+    out, lse = run_paged(case, page_size)
+    check(case, out, lse)
+
+
 @pytest.mark.parametrize("page_size", [64, 16])
 def test_paged_dominant_key_correction(page_size):
     # One term plus the dominant key's correction, whose value row is read
