@@ -347,7 +347,8 @@ int run(const Call& c) {
     if (encode(d, &map_kvo, kv, 4, dims, strides, box_o) != MLA_OK) return MLA_ERR_LAUNCH;
   }
   // Results: fp32 [slice][stream][q*H rows][512] (the slice partials, or `out`
-  // itself when the key range is not split), stored in [128 rows][32] boxes.
+  // itself when the key range is not split), stored in [32 rows][32] boxes
+  // (one per warp of the epilogue).
   float* const part_o = static_cast<float*>(workspace);
   CUtensorMap map_out;
   {
@@ -356,7 +357,7 @@ int run(const Call& c) {
                                 static_cast<cuuint64_t>(ns)};
     const cuuint64_t strides[3] = {512 * 4, static_cast<cuuint64_t>(rps) * 512 * 4,
                                    static_cast<cuuint64_t>(rows) * 512 * 4};
-    const cuuint32_t box[4] = {32, mla::kRows, 1, 1};
+    const cuuint32_t box[4] = {32, 32, 1, 1};
     if (encode(d, &map_out, ns > 1 ? static_cast<void*>(part_o) : static_cast<void*>(out), 4, dims,
                strides, box, CU_TENSOR_MAP_DATA_TYPE_FLOAT32) != MLA_OK)
       return MLA_ERR_LAUNCH;

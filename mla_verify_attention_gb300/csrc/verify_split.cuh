@@ -994,7 +994,13 @@ __device__ __forceinline__ void o_helpers(Smem& sm, const Unit& u, const SplitPa
     else
       p.part_ml[static_cast<size_t>(u.sp) * p.B * u.rows_total + grow] = ml;
   }
-  const bool issuer = wq == 0 && lane == 0;
+  // Each warp stages and stores its own 32 rows (one [32 rows][32 columns]
+  // TMA box per block), without waiting for the other warps; a warp whose rows
+  // all lie past the stream's rows has nothing to store.
+  if (32 * wq >= u.valid_rows) {
+    tc_fence_before();
+    return;
+  }
   // Tensor-memory loads run one block ahead: block cc+1 is requested before
   // block cc is staged (tcgen05.wait::ld then waits for it at the next step).
   uint32_t va[32], vb[32];
@@ -1008,10 +1014,10 @@ __device__ __forceinline__ void o_helpers(Smem& sm, const Unit& u, const SplitPa
     uint32_t* vn = (cc & 1) ? va : vb;
     if (cc + 1 < 8) MLA_TMEM_LD_32x32b_X32(tmem + lane_base + col0 + 32 * (cc + 1), vn);
     if (cc == kOutBufs) {
-      // Blocks 0 and 1 reuse their staging buffers: their stores must have
-      // read them (at most kOutBufs - 2 of this thread's groups still reading).
-      if (issuer) bulk_wait_read<kOutBufs - 2>();
-      named_bar_sync(bar, kRows);
+      // Blocks 0 and 1 reuse their staging buffers: this warp's stores must
+      // have read them (at most kOutBufs - 2 of its groups still reading).
+      if (lane == 0) bulk_wait_read<kOutBufs - 2>();
+      __syncwarp();
     }
     if (kCorrect && need) {
       // Block cc of the warp's value rows: loaded lanes -> buffer (row-major,
@@ -1047,16 +1053,16 @@ __device__ __forceinline__ void o_helpers(Smem& sm, const Unit& u, const SplitPa
           make_float4(__uint_as_float(v[4 * e]) * scale_out, __uint_as_float(v[4 * e + 1]) * scale_out,
                       __uint_as_float(v[4 * e + 2]) * scale_out, __uint_as_float(v[4 * e + 3]) * scale_out);
     fence_proxy_async_smem();
-    named_bar_sync(bar, kRows);
-    if (issuer) {
-      tma_store_4d(map_out, smem_u32(blk), static_cast<int>(col0) + 32 * cc, u.row0, u.b,
-                   direct ? 0 : u.sp);
+    __syncwarp();
+    if (lane == 0) {
+      tma_store_4d(map_out, smem_u32(blk + wq * 32 * 128), static_cast<int>(col0) + 32 * cc,
+                   u.row0 + 32 * wq, u.b, direct ? 0 : u.sp);
       bulk_commit_group();
     }
     if (cc + 1 < 8) tmem_ld_wait();
   }
-  if (issuer) bulk_wait_all();
-  if (issuer && half == 0) MLA_TRACE_SPAN(kSpEpiDone);
+  if (lane == 0) bulk_wait_all();
+  if (wq == 0 && lane == 0 && half == 0) MLA_TRACE_SPAN(kSpEpiDone);
   tc_fence_before();
 }
 
