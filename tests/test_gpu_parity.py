@@ -269,6 +269,8 @@ def test_smax_not_multiple_of_tile(B, prefixes, nsplit):
 @pytest.mark.parametrize("B,prefixes,planted,factor,seed", [
     (1, [65536], [(0, 40000)], 8.0, 21),
     (1, [65536], [(0, 61000)], 10.0, 22),
+    (1, [65536], [(0, 30000)], 20.0, 31),
+    (1, [65536], [(0, 0)], 20.0, 32),          # a sink at the first cache row
     (1, [39991], [(0, 20000)], 8.0, 23),
     (1, [39991], [(0, 39000)], 10.0, 24),
     (8, [1500, 40000, 3000, 9000, 20000, 1100, 30000, 6000],
