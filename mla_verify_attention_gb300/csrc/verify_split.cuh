@@ -93,12 +93,14 @@ constexpr int kOutBufs = 6;                      // staging blocks per helper ha
 static_assert(2 * kOutBufs * kOutBlock <= kRingBytes, "epilogue staging must fit the ring");
 constexpr int kRowThreads = 256;                 // two threads per row (one per 32-key half)
 constexpr uint32_t kQCols = 288;                 // Q in tensor memory: 576 bf16 = 288 cols
-// Dominant-key correction (kCorrect): a key is skipped when its P is below
-// 2^-kCorrKeepLog2 of its half's running sum, and a row's correction when its
-// error is not above 2^-kCorrSkipLog2 of the row sum; either way a skipped
-// term moves the output by at most 2^-13 of a value entry.
-constexpr float kCorrKeepLog2 = 4.0f;
+// Dominant-key correction (kCorrect): a row's correction is skipped when its
+// error is not above 2^-kCorrSkipLog2 of the row sum; a skipped term moves the
+// output by at most 2^-13 of a value entry.
 constexpr float kCorrSkipLog2 = 13.0f;
+// kCorrect, S CTA: the scores of the tile that holds each row half's largest
+// score are kept (128 bytes per row half, 16-byte units XOR-swizzled by row)
+// in the second P term's space of the two P buffers, unused with one term.
+constexpr int kTopScoresOffset = kPOffset + kPHead + kPTerm;   // + half * kPBuf
 // Per helper warp: 32 rows x 64 bytes of value rows, the transpose buffer of
 // the correction's coalesced loads, after the epilogue's staging blocks.
 constexpr int kCorrBufOffset = 2 * kOutBufs * kOutBlock;
@@ -198,8 +200,7 @@ struct __align__(1024) Smem {
   float2 ml[kRows];
   float xmax[2][kRows];      // S CTA: per-half partial row max of the current tile
   float xl[kRows];           // S CTA: second half's running sum, combined at the end
-  float2 xbest[kRows];       // S CTA: second half's {largest score, its P error}
-  int xkey[kRows];           //   and that key (kCorrect)
+  float2 xbest[2][kRows];    // S CTA, per half: {largest score, its key} (kCorrect)
   float2 corr[kRows];        // O CTA: {P error, key} of the row's dominant key (kCorrect)
   uint64_t kfull[2][kKSlots], kempty[2][kKSlots];   // [part][slot]
   uint64_t qfull, qready;
@@ -490,7 +491,8 @@ __device__ __forceinline__ void s_mma(Smem& sm, const Unit& u, const SplitParams
 // tile, the second keys 32..63.  The two halves agree on the row max through
 // shared memory once per tile; each keeps its own part of the running sum.
 // kTwoTerm: P goes out as two bf16 terms hi + lo (short streams).
-// kCorrect: one term, plus the dominant key's rounding error for the O CTA.
+// kCorrect: one term, plus the row's top key and its P's rounding error for
+// the O CTA.
 template <bool kTwoTerm, bool kCorrect>
 __device__ __forceinline__ void s_softmax(Smem& sm, const Unit& u, const SplitParams& p,
                                           uint32_t tmem, int wq, int half, int lane) {
@@ -551,11 +553,15 @@ __device__ __forceinline__ void s_softmax(Smem& sm, const Unit& u, const SplitPa
   float l = 0.f;                  // this half's running sum of P
   bool copy_failed = false;       // set by the copy-issuing thread only
   bool finished = true;
-  // kCorrect: this half's largest log2-scaled score so far, its key and the
-  // rounding error p - bf16(p) of the P staged for it (in O's current scale).
-  float best_x = -CUDART_INF_F;
-  float best_e = 0.f;
-  int best_key = 0;
+  // kCorrect: this half's largest score (before the scale) since its row's
+  // max last changed, and its tile, whose scores the top-scores area keeps.
+  // The key's P was staged with the final max, so its rounding error follows
+  // from the score alone once the loop is done; tracking costs a compare per
+  // tile and a store of 32 scores when a row half sees a new top score
+  // (searching for the key in every such tile slowed the loop by ~8 %).
+  float best_raw = -CUDART_INF_F;
+  int best_j = 0;
+  uint8_t* const top_scores = sm.ring + kTopScoresOffset + half * kPBuf + r * 128;
 
   // Stage P (and the row sums) for 8 keys at a time into exchange buffer `xb`
   // [alpha | flags | P hi | P lo] with exponent offset msub; returns the sum.
@@ -673,7 +679,7 @@ __device__ __forceinline__ void s_softmax(Smem& sm, const Unit& u, const SplitPa
         flag = (m_used != -CUDART_INF_F);  // an all-zero O row needs no rescale
         m_used = mt;
         l *= alpha;
-        if (kCorrect) best_e *= alpha;
+        if (kCorrect) best_raw = -CUDART_INF_F;   // restart under the new max (re-taken below)
       }
       lsum = stage_p(sr, xb, m_used == -CUDART_INF_F ? 0.f : m_used);
       if (half == 0) {
@@ -696,35 +702,39 @@ __device__ __forceinline__ void s_softmax(Smem& sm, const Unit& u, const SplitPa
         copy_failed = true;
       }
     }
-    if (kCorrect && mh > best_x) {
-      // A new largest score of this half (after the copy is on its way):
-      // recompute its P exactly as staged (same fused multiply-add and exp2).
-      // Kept, with its bf16 rounding error, when P is not below 2^-4 of the
-      // running sum (this tile included): a smaller share can only shrink.
-      // (A test against the exponent bits of l instead of the exp2 kept keys
-      // down to l / 32, ran the search below more often and was slower.)
-      const float msub = m_used == -CUDART_INF_F ? 0.f : m_used;
-      const float pv = ex2(fmaf(mraw, a_eff, -msub));
-      best_x = mh;
-      if (pv >= l * exp2f(-kCorrKeepLog2)) {
-        int cb = 0;
+    if (kCorrect && mraw > best_raw) {
+      best_raw = mraw;
+      best_j = j;
 #pragma unroll
-        for (int c = 31; c >= 0; --c)
-          if (__uint_as_float(sr[c]) == mraw) cb = c;
-        best_e = pv - bf16lo_to_f32(pack_bf16x2(pv, pv));
-        best_key = u.k0 + j * kKeys + 32 * half + cb;
-      }
+      for (int q4 = 0; q4 < 8; ++q4)
+        *reinterpret_cast<uint4*>(top_scores + ((q4 ^ (r & 7)) << 4)) =
+            make_uint4(sr[4 * q4], sr[4 * q4 + 1], sr[4 * q4 + 2], sr[4 * q4 + 3]);
     }
   }
   if (half == 0 && r == 0) bulk_wait_read<0>();
   if (wq == 0 && half == 0 && lane == 0) MLA_TRACE_SPAN(kSpLoopDone);
   if (!finished) return;
-  if (half == 1) {
-    sm.xl[r] = l;
-    if (kCorrect) {
-      sm.xbest[r] = make_float2(best_x, best_e);
-      sm.xkey[r] = best_key;
+  if (half == 1) sm.xl[r] = l;
+  if (kCorrect) {
+    // This half's key: the first of its kept scores equal to its top score.
+    int key = -1;
+    if (best_raw != -CUDART_INF_F) {
+      uint32_t v[32];
+#pragma unroll
+      for (int q4 = 0; q4 < 8; ++q4) {
+        const uint4 x = *reinterpret_cast<const uint4*>(top_scores + ((q4 ^ (r & 7)) << 4));
+        v[4 * q4] = x.x;
+        v[4 * q4 + 1] = x.y;
+        v[4 * q4 + 2] = x.z;
+        v[4 * q4 + 3] = x.w;
+      }
+      int cb = -1;
+#pragma unroll
+      for (int c = 31; c >= 0; --c)
+        if (__uint_as_float(v[c]) == best_raw) cb = c;
+      if (cb >= 0) key = u.k0 + best_j * kKeys + 32 * half + cb;
     }
+    sm.xbest[half][r] = make_float2(best_raw, __int_as_float(key));
   }
   if (named_bar_red_or(kSoftmaxBar, kRowThreads, copy_failed)) return;
   if (half == 0) {
@@ -732,13 +742,19 @@ __device__ __forceinline__ void s_softmax(Smem& sm, const Unit& u, const SplitPa
     st_async_v2(mapa_shared(smem_u32(&sm.ml[r]), peer), __float_as_uint(m_used),
                 __float_as_uint(l + sm.xl[r]), mlfull_remote);
     if (kCorrect) {
-      const float2 other = sm.xbest[r];
-      if (other.x > best_x) {
-        best_e = other.y;
-        best_key = sm.xkey[r];
+      // The row's key: the larger of the halves' top scores (the first half on
+      // ties), and the rounding error of its P, recomputed exactly as staged
+      // (same fused multiply-add and exp2, with the final max).
+      const float2 b0 = sm.xbest[0][r], b1 = sm.xbest[1][r];
+      const bool h1 = b1.x > b0.x;
+      const int key = __float_as_int(h1 ? b1.y : b0.y);
+      float e = 0.f;
+      if (key >= 0) {
+        const float pc = ex2(fmaf(h1 ? b1.x : b0.x, a_eff, -m_used));
+        e = pc - bf16lo_to_f32(pack_bf16x2(pc, pc));
       }
-      st_async_v2(mapa_shared(smem_u32(&sm.corr[r]), peer), __float_as_uint(best_e),
-                  static_cast<uint32_t>(best_key), mlfull_remote);
+      st_async_v2(mapa_shared(smem_u32(&sm.corr[r]), peer), __float_as_uint(e),
+                  static_cast<uint32_t>(key >= 0 ? key : 0), mlfull_remote);
     }
   }
 }
