@@ -208,6 +208,22 @@ int mla_verify_attn_plan(int B, int q_len, int H, int Smax, int max_clusters, in
 int mla_verify_attn_set_timing_events(cudaEvent_t before_split, cudaEvent_t after_split);
 
 /*
+ * Precision control; the pages have no counterpart (their kernels keep P in
+ * fp32).  V is bf16 in the cache and the tensor-core product takes P and V in
+ * one type, so P is rounded to bf16.  Streams of at most `max_keys` keys
+ * (seq_lens[b] <= max_keys) send P as two bf16 terms, hi + lo, and run the
+ * P.V product once per term: outputs then match fp32 P to ~1e-5.  Longer
+ * streams send one term and remove the rounding of each row's largest-score
+ * key; a row whose weight several strong keys share keeps the others'
+ * rounding (up to ~2^-9 of a value entry), which two terms remove at the cost
+ * of the second product (the 64k-key, 9-draft call takes ~36 % longer).
+ * Default 4096; 0 sends one term for every stream; INT_MAX two terms for every
+ * stream.  Process-wide, for calls enqueued after it returns.  Returns MLA_OK,
+ * or MLA_ERR_ARG for a negative `max_keys`.  Host-only.
+ */
+int mla_verify_attn_set_two_term_max_keys(int max_keys);
+
+/*
  * Test controls; the pages have no counterpart.  Process-wide settings that
  * every later call reads (a relaxed atomic load per call, no environment
  * lookup), meant for the library's own tests:

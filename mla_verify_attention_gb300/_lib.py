@@ -22,7 +22,8 @@ STATUS_NAMES = {
 EXPORTED = ("mla_verify_attn", "mla_verify_attn_workspace_size", "mla_verify_attn_last_device_error",
             "mla_verify_attn_strerror", "mla_verify_attn_plan", "mla_verify_attn_paged",
             "mla_verify_attn_paged_workspace_size", "mla_verify_attn_set_timing_events",
-            "mla_verify_attn_set_test_controls", "mla_verify_attn_noalloc")
+            "mla_verify_attn_set_test_controls", "mla_verify_attn_noalloc",
+            "mla_verify_attn_set_two_term_max_keys")
 
 _lock = threading.Lock()
 _lib = None
@@ -63,6 +64,8 @@ def load_library(build_if_missing: bool = True) -> ctypes.CDLL:
         lib.mla_verify_attn_set_timing_events.restype = I
         lib.mla_verify_attn_set_test_controls.argtypes = [I, I]
         lib.mla_verify_attn_set_test_controls.restype = I
+        lib.mla_verify_attn_set_two_term_max_keys.argtypes = [I]
+        lib.mla_verify_attn_set_two_term_max_keys.restype = I
         lib.mla_verify_attn_noalloc.argtypes = [P, P, P, P, P, I, I, I, I, F, P, P, P]
         lib.mla_verify_attn_noalloc.restype = I
         _lib = lib
@@ -202,6 +205,19 @@ def set_timing_events(before=None, after=None) -> None:
     st = int(load_library().mla_verify_attn_set_timing_events(b or None, a or None))
     if st != MLA_OK:
         raise MLAError(st, "mla_verify_attn_set_timing_events")
+
+
+TWO_TERM_MAX_KEYS_DEFAULT = 4096
+
+
+def set_two_term_max_keys(max_keys: int) -> None:
+    """Streams of at most ``max_keys`` keys send P as two bf16 terms (exact to
+    ~1e-5); longer ones send one term plus the correction of each row's
+    largest-score key.  Default 4096; 0 = one term everywhere; 2**31 - 1 = two
+    terms everywhere.  Process-wide, for later calls."""
+    st = int(load_library().mla_verify_attn_set_two_term_max_keys(int(max_keys)))
+    if st != MLA_OK:
+        raise MLAError(st, "mla_verify_attn_set_two_term_max_keys")
 
 
 _controls = [0, 0]   # the values last given to mla_verify_attn_set_test_controls

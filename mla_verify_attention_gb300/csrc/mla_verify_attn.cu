@@ -33,7 +33,8 @@ constexpr int kMinTilesPerSlice = mla::kMinSliceTiles;
 // to ~3e-3 into longer streams where one key carries much of a row's weight.
 // Streams up to kTwoTermMaxKeys keys send P as hi + lo (their slices are short,
 // and the second PV product is cheap there); longer ones send one term plus
-// the correction of each row's dominant key (the kCorrect kernel).
+// the correction of each row's dominant key (the kCorrect kernel).  The limit
+// can be moved with mla_verify_attn_set_two_term_max_keys.
 constexpr int kTwoTermMaxKeys = 4096;
 constexpr size_t kSmemBytes = sizeof(mla::Smem) + 1024;   // + manual 1 KB alignment
 
@@ -57,6 +58,8 @@ cudaEvent_t g_timing_after = nullptr;
 // (0 = the plan's own) and the stall of one work unit; plain loads per call.
 std::atomic<int> g_force_nsplit{0};
 std::atomic<int> g_test_stall{0};
+// Longest stream that sends P as two terms (mla_verify_attn_set_two_term_max_keys).
+std::atomic<int> g_two_term_max_keys{kTwoTermMaxKeys};
 
 int device_info(DeviceInfo** out) {
   int dev = -1;
@@ -384,7 +387,7 @@ int run(const Call& c) {
                                 : nullptr;
   p.plan = plan_dev;
   const bool corrected = true;
-  const int two_term_max_keys = kTwoTermMaxKeys;
+  const int two_term_max_keys = g_two_term_max_keys.load(std::memory_order_relaxed);
   p.two_term_max_keys = two_term_max_keys;
   p.kv = static_cast<const uint8_t*>(kv);
   p.kv_rows = paged ? c.pool_rows : static_cast<long long>(Smax);
@@ -566,6 +569,12 @@ int mla_verify_attn_trace_read(unsigned long long* tiles, unsigned long long* sp
   return MLA_OK;
 }
 #endif
+
+int mla_verify_attn_set_two_term_max_keys(int max_keys) {
+  if (max_keys < 0) return MLA_ERR_ARG;
+  g_two_term_max_keys.store(max_keys, std::memory_order_relaxed);
+  return MLA_OK;
+}
 
 int mla_verify_attn_set_test_controls(int force_nsplit, int stall) {
   if (force_nsplit < 0) return MLA_ERR_ARG;

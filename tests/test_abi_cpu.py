@@ -102,6 +102,14 @@ def test_forced_slice_count(lib, monkeypatch):
     assert mva.plan(1, 9, 64, 4160, 76) == (5, 13, 5)
 
 
+def test_two_term_limit_setter(lib):
+    assert lib.mla_verify_attn_set_two_term_max_keys(-1) == -9   # MLA_ERR_ARG
+    with pytest.raises(mva.MLAError):
+        mva.set_two_term_max_keys(-5)
+    for v in (0, 2**31 - 1, mva.TWO_TERM_MAX_KEYS_DEFAULT):
+        mva.set_two_term_max_keys(v)
+
+
 def paged(lib, **kw):
     a = dict(qn=16, qr=16, pool=16, rows=640, bt=16, mb=5, ps=128, sl=16, m=16, B=1, q=9, H=64,
              scale=0.07, out=16, lse=16, ws=0, wsb=0)

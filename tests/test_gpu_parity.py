@@ -284,6 +284,36 @@ def test_dominant_key_in_large_cache(B, prefixes, planted, factor, seed):
     check(case, *run_gpu(case))
 
 
+# ---------------------------------------------------------------- the correction itself
+
+# A key that carries most rows' weight in an 8009-key stream: left uncorrected,
+# its bf16 weight moves outputs by 3e-3 to 6e-3 (past the tolerance) in units
+# of 8, 63 or 126 tiles alike.  Corrected, what remains is the rounding of the
+# other keys' weights (measured 2.6e-4 to 5.1e-4).
+@pytest.mark.parametrize("nsplit", [None, 2, 1])
+def test_dominant_key_rounding_removed(nsplit):
+    case = custom_case(1, 9, 64, [7999], seed=1)
+    I.scale_key_rope(case, 0, 7000, 10.0)
+    d_out, _ = check(case, *run_gpu(case, nsplit=nsplit))
+    assert d_out <= 1e-3, d_out
+
+
+# Weight spread over several strong keys in one long slice: one bf16 term keeps
+# the rounding of all but each row's top key (3.0e-3 measured with 20 planted
+# keys and one 126-tile slice); two terms for every stream remove it.
+def test_two_terms_for_spread_weight():
+    import mla_verify_attention_gb300 as mva
+    case = custom_case(1, 9, 64, [7999], seed=2)
+    for k in range(100, 7900, 397):
+        I.scale_key_rope(case, 0, k, 10.0)
+    mva.set_two_term_max_keys(2**31 - 1)
+    try:
+        d_out, _ = check(case, *run_gpu(case, nsplit=1))
+    finally:
+        mva.set_two_term_max_keys(mva.TWO_TERM_MAX_KEYS_DEFAULT)
+    assert d_out <= 5e-4, d_out
+
+
 # ---------------------------------------------------------------- full-size workloads
 
 @pytest.mark.parametrize("name", ["tree33_p16384", "tree9_p65536", "ragged8_tree9"])
