@@ -1088,8 +1088,10 @@ __device__ __forceinline__ void o_helpers(Smem& sm, const Unit& u, const SplitPa
 //   kDepNone: plain stream order.
 //   kDepCopy: programmatic dependent of the grid that copied a paged cache into
 //     a contiguous one; only the cache loads wait for that grid.
-//   kDepPlan: programmatic dependent of plan_kernel; every thread waits for the
-//     plan before decoding its unit (its launch overlaps the planner's run).
+//   kDepPlan: programmatic dependent of the grid before it (plan_kernel, or
+//     any other); every thread waits for that grid before reading anything.
+//     (The plan is then ready; and a dependent launch starts sooner after the
+//     grid before it ends than a plain one, with the same ordering.)
 // (Separate instantiations: the wait instruction in the kernel cost ~0.7 us per
 // call even when not executed.)  kCorrect: units that send one P term also
 // remove their dominant keys' rounding (a separate instantiation too, so that
@@ -1106,7 +1108,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   Smem& sm = *reinterpret_cast<Smem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                       ~static_cast<uintptr_t>(1023));
   constexpr bool kAfterCopy = kDep == kDepCopy;
-  if (kDep == kDepPlan) grid_dependency_wait();   // the plan is the preceding grid's output
+  if (kDep == kDepPlan) grid_dependency_wait();   // the preceding grid (the plan, if any) is done
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
   const int lane = tid & 31;
