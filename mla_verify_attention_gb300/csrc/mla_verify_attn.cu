@@ -411,9 +411,21 @@ int run(const Call& c) {
     rp.page_size = c.page_size;
     rp.pool_pages = static_cast<int>(c.pool_rows / c.page_size);
     rp.Smax = Smax;
-    const dim3 grid((Smax + mla::kKeys - 1) / mla::kKeys, B < 65535 ? B : 65535, 1);
-    mla::repack_kernel<<<grid, mla::kRepackThreads, 0, stream>>>(rp);
-    if (cudaGetLastError() != cudaSuccess) return MLA_ERR_LAUNCH;
+    // A programmatic dependent of the grid before it (it waits for that grid first).
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((Smax + mla::kKeys - 1) / mla::kKeys, B < 65535 ? B : 65535, 1);
+    cfg.blockDim = dim3(mla::kRepackThreads, 1, 1);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaLaunchKernelEx(&cfg, mla::repack_kernel, rp) != cudaSuccess) {
+      cudaGetLastError();
+      return MLA_ERR_LAUNCH;
+    }
   }
   if (planned) {
     mla::PlanParams pp;
@@ -428,8 +440,22 @@ int run(const Call& c) {
     pp.slots = d->max_clusters;
     pp.two_term_max_keys = two_term_max_keys;
     const int ncand = ns < mla::kPlanMaxCandidates ? ns : mla::kPlanMaxCandidates;
-    mla::plan_kernel<<<1, 32 * ncand, 0, stream>>>(pp);
-    if (cudaGetLastError() != cudaSuccess) return MLA_ERR_LAUNCH;
+    // A programmatic dependent of the grid before it (it waits for that grid
+    // first), so that its launch overlaps that grid's end.
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(1, 1, 1);
+    cfg.blockDim = dim3(static_cast<unsigned>(32 * ncand), 1, 1);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaLaunchKernelEx(&cfg, mla::plan_kernel, pp) != cudaSuccess) {
+      cudaGetLastError();
+      return MLA_ERR_LAUNCH;
+    }
   }
   const bool timing = g_timing_before != nullptr;
   // The split kernel is a programmatic dependent of the grid before it: of

@@ -47,8 +47,11 @@ __device__ __forceinline__ unsigned plan_time(float us) { return static_cast<uns
 __global__ void __launch_bounds__(32 * kPlanMaxCandidates, 1) plan_kernel(const PlanParams p) {
   __shared__ unsigned cost[kPlanMaxCandidates];
   __shared__ int chunk_of[kPlanMaxCandidates];
-  // The split kernel is this grid's programmatic dependent: it may be
-  // scheduled now and waits for this grid's completion before reading the plan.
+  // This grid is itself a programmatic dependent of the grid before it: wait
+  // for that grid before reading the stream lengths.  The split kernel is this
+  // grid's programmatic dependent: it may be scheduled now and waits for this
+  // grid's completion before reading the plan.
+  grid_dependency_wait();
   if (threadIdx.x == 0) grid_launch_dependents();
   const int lane = threadIdx.x & 31;
   const int warp = threadIdx.x >> 5;

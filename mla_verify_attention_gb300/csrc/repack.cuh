@@ -42,9 +42,11 @@ static_assert(kRepackPieces % (kRepackBatch * kRepackThreads) == 0, "repack batc
 __global__ void __launch_bounds__(kRepackThreads, 4) repack_kernel(const RepackParams p) {
   __shared__ int32_t rows[kKeys];
   const int t = threadIdx.x;
-  // The split kernel is launched as a programmatic dependent: its CTAs may
-  // start (Q loads, tensor-memory setup) while the last copies run; its cache
-  // loads wait for this grid's completion.
+  // This grid is a programmatic dependent of the grid before it: wait for
+  // that grid before reading anything.  The split kernel is this grid's
+  // programmatic dependent: its CTAs may start (Q loads, tensor-memory setup)
+  // while the last copies run; its cache loads wait for this grid's completion.
+  grid_dependency_wait();
   if (t == 0) grid_launch_dependents();
   const int key0 = blockIdx.x * kKeys;
   for (int b = blockIdx.y; b < p.B; b += gridDim.y) {
