@@ -530,11 +530,22 @@ int run(const Call& c) {
     // Slices per load batch: 16 while all rows fit one wave at four blocks per
     // SM, else 8 (more resident rows; batches are merged online).
     const int nb = ns <= 4 ? 4 : ((ns <= 8 || rows > 4LL * d->sms) ? 8 : 16);
-    // Few rows and many slices (e.g. 8 heads over a long stream): four groups
-    // of threads per row share the slices.
+    // Few rows and many slices (e.g. 8 or 16 heads over a long stream): the
+    // slices of a row are shared by groups of threads.  While four blocks of
+    // 128 columns per row fit one wave (two per SM), sixteen groups per block
+    // (one round of loads for up to 96 slices: H = 8 at 64k keys 33.7 -> 31.1
+    // us/call); otherwise one block per row of four 128-thread groups (at 16
+    // heads the column split took 2 waves and was 1.8 us slower).
     const bool grouped = ns > 16 && rows <= d->sms;
-    if (grouped) cfg.blockDim = dim3(4 * 128, 1, 1);
-    if (cudaLaunchKernelEx(&cfg, grouped ? mla::combine_kernel<16, 4>
+    const bool cols = grouped && 4 * rows <= 2LL * d->sms;
+    if (cols) {
+      cfg.gridDim = dim3(static_cast<unsigned>(rows), 4, 1);
+      cfg.blockDim = dim3(16 * 32, 1, 1);
+    } else if (grouped) {
+      cfg.blockDim = dim3(4 * 128, 1, 1);
+    }
+    if (cudaLaunchKernelEx(&cfg, cols ? mla::combine_cols_kernel<6, 16, 4>
+                                 : grouped ? mla::combine_kernel<16, 4>
                                  : (nb == 4 ? mla::combine_kernel<4, 1>
                                             : (nb == 8 ? mla::combine_kernel<8, 1> : mla::combine_kernel<16, 1>)),
                            c) != cudaSuccess) {

@@ -52,6 +52,7 @@ KERNEL_ROLES = (
     ("verify_split_kernel", "split kernel: QK, mask, online softmax and PV of one key slice "
                             "per 2-CTA cluster"),
     ("combine_kernel", "merge of the slices' partial states"),
+    ("combine_cols_kernel", "merge of the slices' partial states (few rows: 128-column blocks)"),
     ("plan_kernel", "device-side slice plan (2..32 streams)"),
     ("repack_kernel", "copy of a paged cache into a contiguous one"),
 )
