@@ -38,11 +38,12 @@
 // max even the dominant key's p carries that rounding, so streams up to
 // two_term_max_keys keys (where a few keys carry most of the weight) send P as
 // two bf16 terms hi + lo and the PV product is issued once per term.  The
-// kCorrect instantiation (caches of up to 32768 keys) sends one term for the
-// longer of those streams and removes the dominant key's rounding instead:
-// the softmax threads keep, per row, the key with the largest score and the
-// error p - bf16(p) of its P (rescaled with O), and the O CTA adds error x
-// that key's value row to the accumulator before the epilogue.
+// kCorrect instantiation sends one term for longer streams and removes the
+// dominant key's rounding instead: each softmax thread tracks its largest
+// score since its row's max last changed and keeps that half tile's scores,
+// finds the key after the loop and recomputes the error p - bf16(p) of its P,
+// and the O CTA adds error x that key's value row to the accumulator before
+// the epilogue.
 //
 // Units start in index order.  For 2..32 streams the index order is a list
 // schedule (ordered_slice), and the slice length may come from plan_kernel
