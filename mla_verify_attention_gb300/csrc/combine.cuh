@@ -38,11 +38,122 @@ __device__ __forceinline__ void wait_for_split_grid() {
   asm volatile("griddepcontrol.wait;" ::: "memory");
 }
 
-// kBatch 16: four blocks per SM (<= 128 registers), all rows of a 64-head,
-// 9-draft call in one wave; kBatch 8 and 4: 6 and 12 blocks per SM.
-// kGroups > 1 (calls with few rows and many slices, e.g. 8 heads): each of
-// kGroups groups of 128 threads merges every kGroups-th slice of the row, and
-// the groups' states are merged through shared memory at the end.
+// Running state of one row's merge: max M (log2 units), sum L and four
+// accumulator columns.
+struct MergeState {
+  float M, L;
+  float4 acc;
+};
+
+__device__ __forceinline__ MergeState empty_state() {
+  MergeState st;
+  st.M = -CUDART_INF_F;
+  st.L = 0.f;
+  st.acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  return st;
+}
+
+// The row's slice count, or -1 for a stream length the split kernel reported.
+__device__ __forceinline__ int row_slices(const CombineParams& p, int row) {
+  const int S = p.seq_lens[row / p.rows_per_stream];
+  if (S < p.q || S > p.Smax) return -1;
+  const int chunk_keys = p.plan != nullptr ? p.plan[0] * 64 : p.chunk_keys;
+  return min(p.plan != nullptr ? p.plan[1] : p.nsplit, (S + chunk_keys - 1) / chunk_keys);
+}
+
+// Slices first, first + stride, ... (< ns) of one row into `st`.  Every slice
+// wrote its partial (an all-zero accumulator where no key was visible).  A
+// batch's (m, l) pairs and accumulators are all requested before any is used;
+// batches are merged online.  `ml` and `src` point at slice 0 of the row.
+template <int kBatch>
+__device__ __forceinline__ void merge_slices(MergeState& st, const float2* ml, const float4* src,
+                                             int N, int ns, int first, int stride) {
+  const size_t step4 = static_cast<size_t>(N) * 128;   // float4s between slices
+  for (int s0 = first; s0 < ns; s0 += kBatch * stride) {
+    float2 v[kBatch];
+    float4 o[kBatch];
+#pragma unroll
+    for (int e = 0; e < kBatch; ++e) {
+      const int s = s0 + e * stride;
+      if (s < ns) {
+        v[e] = ml[static_cast<size_t>(s) * N];
+        o[e] = src[s * step4];
+      } else {
+        v[e] = make_float2(-CUDART_INF_F, 0.f);
+        o[e] = make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+    }
+    float Mb = st.M;
+#pragma unroll
+    for (int e = 0; e < kBatch; ++e) Mb = v[e].y > 0.f ? fmaxf(Mb, v[e].x) : Mb;
+    if (Mb == -CUDART_INF_F) continue;            // nothing visible so far
+    const float c = ex2(st.M - Mb);               // 0 while M = -inf (L, acc are 0 then)
+    st.L *= c;
+    st.acc.x *= c; st.acc.y *= c; st.acc.z *= c; st.acc.w *= c;
+#pragma unroll
+    for (int e = 0; e < kBatch; ++e) {
+      const float w = v[e].y > 0.f ? ex2(v[e].x - Mb) : 0.f;
+      st.L += w * v[e].y;
+      st.acc.x += w * o[e].x;
+      st.acc.y += w * o[e].y;
+      st.acc.z += w * o[e].z;
+      st.acc.w += w * o[e].w;
+    }
+    st.M = Mb;
+  }
+}
+
+// The states of kGroups groups of kLanes threads (thread t of group g holds
+// columns t) merged through shared memory into group 0's threads; the other
+// groups' threads get false and are done.  Every thread of the block calls it.
+template <int kGroups, int kLanes>
+__device__ __forceinline__ bool merge_groups(MergeState& st, int grp, int t) {
+  __shared__ float gm[kGroups], gl[kGroups];
+  __shared__ float4 gacc[kGroups][kLanes];
+  if (t == 0) {
+    gm[grp] = st.M;
+    gl[grp] = st.L;
+  }
+  gacc[grp][t] = st.acc;
+  __syncthreads();
+  if (grp != 0) return false;
+  st = empty_state();
+#pragma unroll
+  for (int g = 0; g < kGroups; ++g) st.M = gl[g] > 0.f ? fmaxf(st.M, gm[g]) : st.M;
+  if (st.M != -CUDART_INF_F) {
+#pragma unroll
+    for (int g = 0; g < kGroups; ++g) {
+      const float w = gl[g] > 0.f ? ex2(gm[g] - st.M) : 0.f;
+      const float4 a = gacc[g][t];
+      st.L += w * gl[g];
+      st.acc.x += w * a.x;
+      st.acc.y += w * a.y;
+      st.acc.z += w * a.z;
+      st.acc.w += w * a.w;
+    }
+  }
+  return true;
+}
+
+// Four columns (float4 `col4`) of the normalised output row, and its lse when
+// `lse_writer`; an empty row gives out = 0 and lse = -inf.
+__device__ __forceinline__ void write_row(const CombineParams& p, int row, int col4,
+                                          const MergeState& st, bool lse_writer) {
+  float4* dst = reinterpret_cast<float4*>(p.out + static_cast<size_t>(row) * 512) + col4;
+  if (st.M == -CUDART_INF_F) {
+    *dst = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (lse_writer) p.lse[row] = -CUDART_INF_F;
+    return;
+  }
+  const float inv = 1.f / st.L;
+  *dst = make_float4(st.acc.x * inv, st.acc.y * inv, st.acc.z * inv, st.acc.w * inv);
+  if (lse_writer) p.lse[row] = (st.M + log2f(st.L)) * 0.6931471805599453f;
+}
+
+// One block of 128 * kGroups threads per row.  kBatch 16: four blocks per SM
+// (<= 128 registers), all rows of a 64-head, 9-draft call in one wave; kBatch
+// 8 and 4: 6 and 12 blocks per SM.  kGroups > 1 (few rows, many slices): each
+// of kGroups groups of 128 threads merges every kGroups-th slice of the row.
 template <int kBatch, int kGroups>
 __global__ void __launch_bounds__(128 * kGroups, kGroups > 1 ? 1 : (kBatch == 16 ? 4 : (kBatch == 8 ? 6 : 12)))
     combine_kernel(const CombineParams p) {
@@ -50,95 +161,21 @@ __global__ void __launch_bounds__(128 * kGroups, kGroups > 1 ? 1 : (kBatch == 16
   const int row = blockIdx.x;
   const int tid = threadIdx.x & 127;
   const int grp = threadIdx.x >> 7;
-  const int b = row / p.rows_per_stream;
-  const int S = p.seq_lens[b];
-  if (S < p.q || S > p.Smax) return;   // reported by the split kernel
-  const int chunk_keys = p.plan != nullptr ? p.plan[0] * 64 : p.chunk_keys;
-  const int ns = min(p.plan != nullptr ? p.plan[1] : p.nsplit, (S + chunk_keys - 1) / chunk_keys);
-  const float2* ml = p.part_ml + row;
-  const float4* src = reinterpret_cast<const float4*>(p.part_o + static_cast<size_t>(row) * 512) + tid;
-  const size_t step4 = static_cast<size_t>(p.N) * 128;   // float4s between slices
-  // Every slice s < ns wrote its partial (an all-zero accumulator where no key
-  // was visible).  A batch's (m, l) pairs and accumulators are all requested
-  // before any is used; batches are merged online (running max M).
-  float M = -CUDART_INF_F, L = 0.f;
-  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-  for (int s0 = grp; s0 < ns; s0 += kBatch * kGroups) {
-    float2 v[kBatch];
-    float4 o[kBatch];
-#pragma unroll
-    for (int e = 0; e < kBatch; ++e) {
-      const int s = s0 + e * kGroups;
-      if (s < ns) {
-        v[e] = ml[static_cast<size_t>(s) * p.N];
-        o[e] = src[s * step4];
-      } else {
-        v[e] = make_float2(-CUDART_INF_F, 0.f);
-        o[e] = make_float4(0.f, 0.f, 0.f, 0.f);
-      }
-    }
-    float Mb = M;
-#pragma unroll
-    for (int e = 0; e < kBatch; ++e) Mb = v[e].y > 0.f ? fmaxf(Mb, v[e].x) : Mb;
-    if (Mb == -CUDART_INF_F) continue;            // nothing visible so far
-    const float c = ex2(M - Mb);                  // 0 while M = -inf (L, acc are 0 then)
-    L *= c;
-    acc.x *= c; acc.y *= c; acc.z *= c; acc.w *= c;
-#pragma unroll
-    for (int e = 0; e < kBatch; ++e) {
-      const float w = v[e].y > 0.f ? ex2(v[e].x - Mb) : 0.f;
-      L += w * v[e].y;
-      acc.x += w * o[e].x;
-      acc.y += w * o[e].y;
-      acc.z += w * o[e].z;
-      acc.w += w * o[e].w;
-    }
-    M = Mb;
-  }
-  if (kGroups > 1) {
-    __shared__ float gm[kGroups], gl[kGroups];
-    __shared__ float4 gacc[kGroups][128];
-    if (tid == 0) {
-      gm[grp] = M;
-      gl[grp] = L;
-    }
-    gacc[grp][tid] = acc;
-    __syncthreads();
-    if (grp != 0) return;
-    M = -CUDART_INF_F;
-#pragma unroll
-    for (int g = 0; g < kGroups; ++g) M = gl[g] > 0.f ? fmaxf(M, gm[g]) : M;
-    L = 0.f;
-    acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (M != -CUDART_INF_F) {
-#pragma unroll
-      for (int g = 0; g < kGroups; ++g) {
-        const float w = gl[g] > 0.f ? ex2(gm[g] - M) : 0.f;
-        const float4 a = gacc[g][tid];
-        L += w * gl[g];
-        acc.x += w * a.x;
-        acc.y += w * a.y;
-        acc.z += w * a.z;
-        acc.w += w * a.w;
-      }
-    }
-  }
-  float4* dst = reinterpret_cast<float4*>(p.out + static_cast<size_t>(row) * 512) + tid;
-  if (M == -CUDART_INF_F) {
-    *dst = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (tid == 0) p.lse[row] = -CUDART_INF_F;
-    return;
-  }
-  const float inv = 1.f / L;
-  *dst = make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
-  if (tid == 0) p.lse[row] = (M + log2f(L)) * 0.6931471805599453f;
+  const int ns = row_slices(p, row);
+  if (ns < 0) return;   // reported by the split kernel
+  MergeState st = empty_state();
+  merge_slices<kBatch>(st, p.part_ml + row,
+                       reinterpret_cast<const float4*>(p.part_o + static_cast<size_t>(row) * 512) + tid,
+                       p.N, ns, grp, kGroups);
+  if (kGroups > 1 && !merge_groups<kGroups, 128>(st, grp, tid)) return;
+  write_row(p, row, tid, st, tid == 0);
 }
 
-// Few rows and many slices (e.g. 8 or 16 heads over a long stream): each row is
+// Few rows and many slices (e.g. 8 heads over a long stream): each row is
 // merged by kCols blocks of 512 / kCols columns, and in each block kGroups
 // groups of 32 threads (4 columns a thread) merge every kGroups-th slice, so
-// that up to kBatch * kGroups slices' loads are in flight per block at once;
-// the groups' states are merged through shared memory.  Grid (rows, kCols).
+// that up to kBatch * kGroups slices' loads are in flight per block at once.
+// Grid (rows, kCols).
 template <int kBatch, int kGroups, int kCols>
 __global__ void __launch_bounds__(32 * kGroups, 2) combine_cols_kernel(const CombineParams p) {
   static_assert(kCols * 32 * 4 == 512, "one float4 per thread of a 32-thread group");
@@ -146,85 +183,15 @@ __global__ void __launch_bounds__(32 * kGroups, 2) combine_cols_kernel(const Com
   const int row = blockIdx.x;
   const int lane = threadIdx.x & 31;
   const int grp = threadIdx.x >> 5;
-  const int b = row / p.rows_per_stream;
-  const int S = p.seq_lens[b];
-  if (S < p.q || S > p.Smax) return;   // reported by the split kernel
-  const int chunk_keys = p.plan != nullptr ? p.plan[0] * 64 : p.chunk_keys;
-  const int ns = min(p.plan != nullptr ? p.plan[1] : p.nsplit, (S + chunk_keys - 1) / chunk_keys);
-  const float2* ml = p.part_ml + row;
+  const int ns = row_slices(p, row);
+  if (ns < 0) return;   // reported by the split kernel
   const int col4 = blockIdx.y * 32 + lane;                 // float4 column of this thread
-  const float4* src = reinterpret_cast<const float4*>(p.part_o + static_cast<size_t>(row) * 512) + col4;
-  const size_t step4 = static_cast<size_t>(p.N) * 128;   // float4s between slices
-  float M = -CUDART_INF_F, L = 0.f;
-  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-  for (int s0 = grp; s0 < ns; s0 += kBatch * kGroups) {
-    float2 v[kBatch];
-    float4 o[kBatch];
-#pragma unroll
-    for (int e = 0; e < kBatch; ++e) {
-      const int s = s0 + e * kGroups;
-      if (s < ns) {
-        v[e] = ml[static_cast<size_t>(s) * p.N];
-        o[e] = src[s * step4];
-      } else {
-        v[e] = make_float2(-CUDART_INF_F, 0.f);
-        o[e] = make_float4(0.f, 0.f, 0.f, 0.f);
-      }
-    }
-    float Mb = M;
-#pragma unroll
-    for (int e = 0; e < kBatch; ++e) Mb = v[e].y > 0.f ? fmaxf(Mb, v[e].x) : Mb;
-    if (Mb == -CUDART_INF_F) continue;            // nothing visible so far
-    const float c = ex2(M - Mb);                  // 0 while M = -inf (L, acc are 0 then)
-    L *= c;
-    acc.x *= c; acc.y *= c; acc.z *= c; acc.w *= c;
-#pragma unroll
-    for (int e = 0; e < kBatch; ++e) {
-      const float w = v[e].y > 0.f ? ex2(v[e].x - Mb) : 0.f;
-      L += w * v[e].y;
-      acc.x += w * o[e].x;
-      acc.y += w * o[e].y;
-      acc.z += w * o[e].z;
-      acc.w += w * o[e].w;
-    }
-    M = Mb;
-  }
-  __shared__ float gm[kGroups], gl[kGroups];
-  __shared__ float4 gacc[kGroups][32];
-  if (lane == 0) {
-    gm[grp] = M;
-    gl[grp] = L;
-  }
-  gacc[grp][lane] = acc;
-  __syncthreads();
-  if (grp != 0) return;
-  M = -CUDART_INF_F;
-#pragma unroll
-  for (int g = 0; g < kGroups; ++g) M = gl[g] > 0.f ? fmaxf(M, gm[g]) : M;
-  L = 0.f;
-  acc = make_float4(0.f, 0.f, 0.f, 0.f);
-  if (M != -CUDART_INF_F) {
-#pragma unroll
-    for (int g = 0; g < kGroups; ++g) {
-      const float w = gl[g] > 0.f ? ex2(gm[g] - M) : 0.f;
-      const float4 a = gacc[g][lane];
-      L += w * gl[g];
-      acc.x += w * a.x;
-      acc.y += w * a.y;
-      acc.z += w * a.z;
-      acc.w += w * a.w;
-    }
-  }
-  float4* dst = reinterpret_cast<float4*>(p.out + static_cast<size_t>(row) * 512) + col4;
-  const bool lse_writer = blockIdx.y == 0 && lane == 0;
-  if (M == -CUDART_INF_F) {
-    *dst = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (lse_writer) p.lse[row] = -CUDART_INF_F;
-    return;
-  }
-  const float inv = 1.f / L;
-  *dst = make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
-  if (lse_writer) p.lse[row] = (M + log2f(L)) * 0.6931471805599453f;
+  MergeState st = empty_state();
+  merge_slices<kBatch>(st, p.part_ml + row,
+                       reinterpret_cast<const float4*>(p.part_o + static_cast<size_t>(row) * 512) + col4,
+                       p.N, ns, grp, kGroups);
+  if (!merge_groups<kGroups, 32>(st, grp, lane)) return;
+  write_row(p, row, col4, st, blockIdx.y == 0 && lane == 0);
 }
 
 }  // namespace mla
