@@ -314,6 +314,17 @@ def test_two_terms_for_spread_weight():
     assert d_out <= 5e-4, d_out
 
 
+# ---------------------------------------------------------------- merge of many slices, few rows
+
+# 8 or 16 heads over a long stream: more than 16 slices per row.  With at most
+# 76 rows each row is merged by four 128-column blocks of sixteen slice groups;
+# with more rows (16 heads, or two streams of 8) by one block of four groups.
+@pytest.mark.parametrize("B,H,nsplit", [(1, 8, 20), (1, 8, 40), (1, 16, 20), (2, 8, 24)])
+def test_merge_of_many_slices_few_rows(B, H, nsplit):
+    case = custom_case(B, 9, H, [6000] * B, seed=300 + B + H + nsplit)
+    check(case, *run_gpu(case, nsplit=nsplit))
+
+
 # ---------------------------------------------------------------- full-size workloads
 
 @pytest.mark.parametrize("name", ["tree33_p16384", "tree9_p65536", "ragged8_tree9"])
